@@ -1,0 +1,341 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 attention forward (one JSON line on rank 0).
+
+Workload ("S=4K/8K/16K sweep"): one step runs the attention forward once on
+each headline shape -- S=4K (B=4, H=16), S=8K (B=2, H=16), S=16K (B=1, H=16);
+D=128, dense, non-causal, BF16, scale 1/sqrt(128), inputs N(0,1) -- with all
+inputs resident in HBM.  metric: TFLOPS = 4*B*H*Sq*Sk*D summed over the three
+shapes / the summed kernel time, and its fraction of the measured GB300 dense
+BF16 peak.  Every input set (Q+K+V = 192 MiB per shape) is larger than the
+129 MB L2, so no explicit flush is needed between timed iterations.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only reference this path has)
+on bounded samples of the same workload, on the host cores.
+Under torchrun (N > 1) every rank runs the same per-GPU workload on its own
+GPU (replicas, weak scaling); the timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOPS (4·B·H·S²·D) at S=4K/8K/16K, % of GB300 BF16 peak"
+UNIT = "TFLOP/s"
+WORKLOAD = "S=4K/8K/16K sweep (B=4/2/1, H=16, D=128, BF16, non-causal)"
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in a background process."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_attention_forward_attn_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_for(workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on this exact source."""
+    path = os.path.join(ROOT, "profiles", "attn_fwd_kernel_dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("source_sha") != _source_sha():
+            return None
+        return d["per_launch_bytes"].get(workload_name)
+    except Exception:
+        return None
+
+
+def oracle_sample_tflops(shapes, seconds: float, seed: int = 0):
+    """Time the fp64 CPU oracle on random rows of each shape for about `seconds` in total."""
+    import numpy as np
+    import oracle
+    from dense_attention_forward_attn_gb300 import workloads as wl
+
+    total_flops, total_t, rows_done = 0.0, 0.0, []
+    per = seconds / len(shapes)
+    threads = oracle.max_threads()
+    for w, (qb, kb, vb) in shapes:
+        # calibrate with a small batch, then run a batch sized to `per` seconds
+        rng = np.random.Generator(np.random.PCG64(seed))
+        n = max(threads, 16)
+        bh = rng.integers(0, w.B * w.H, n)
+        rows = rng.integers(0, w.Sq, n)
+        t0 = time.perf_counter()
+        oracle.attn_fwd_rows(qb, kb, vb, w.scale, bh, rows)
+        dt = time.perf_counter() - t0
+        n2 = max(threads, int(n * per / max(dt, 1e-6)))
+        bh = rng.integers(0, w.B * w.H, n2)
+        rows = rng.integers(0, w.Sq, n2)
+        t0 = time.perf_counter()
+        oracle.attn_fwd_rows(qb, kb, vb, w.scale, bh, rows)
+        dt = time.perf_counter() - t0
+        total_flops += 4.0 * w.Sk * w.D * n2
+        total_t += dt
+        rows_done.append(f"{n2} rows of {w.name}")
+    return total_flops / total_t / 1e12, threads, ", ".join(rows_done), total_t
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    from dense_attention_forward_attn_gb300 import workloads as wl
+    shapes = [(w, wl.workload_inputs_bits(w)) for w in wl.HEADLINE]
+    step_s = 1.5
+    vals, times = [], []
+    for i in range(args.warmup + args.steps):
+        v, cores, sample, t = oracle_sample_tflops(shapes, step_s, seed=i)
+        if i >= args.warmup:
+            vals.append(v)
+            times.append(t)
+    value = sum(vals) / len(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "reference": "fp64 CPU oracle (oracle/attn_oracle.c), "
+                   "the only reference this path has", "sample": "each step: random query rows "
+                   "of each shape, about 0.5 s of CPU work per shape"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from dense_attention_forward_attn_gb300 import attn, workloads as wl
+
+    shapes = []
+    for w in wl.HEADLINE:
+        qb, kb, vb = wl.workload_inputs_bits(w)
+        host = [wl.bits_to_torch(x).pin_memory() for x in (qb, kb, vb)]
+        d = [t.to(dev) for t in host]
+        o = torch.empty_like(d[0])
+        lse = torch.empty(w.B, w.H, w.Sq, dtype=torch.float32, device=dev)
+        shapes.append((w, (qb, kb, vb), host, d, o, lse))
+    flops = sum(w.flops for w, *_ in shapes)
+    stream = torch.cuda.current_stream()
+    attn.device_status(clear=True)
+
+    def step(evs=None):
+        for i, (w, _, _, d, o, lse) in enumerate(shapes):
+            if evs is not None:
+                evs[i][0].record(stream)
+            attn.fwd_into(d[0], d[1], d[2], o, lse, w.scale)
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    # ---------------- device-resident timed region
+    n = len(shapes)
+    kev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+           for _ in range(args.steps)]
+    clocks = ClockSampler(local if ws > 1 else torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.3)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        step(kev[s])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = ws * flops / (ms_per_step * 1e-3) / 1e12
+    per_cfg = {}
+    kernel_ms_total = 0.0
+    for i, (w, *_rest) in enumerate(shapes):
+        ms = [kev[s][i][0].elapsed_time(kev[s][i][1]) for s in range(args.steps)]
+        avg = sum(ms) / len(ms)
+        kernel_ms_total += avg
+        per_cfg[w.name] = {"ms_avg": round(avg, 4), "ms_min": round(min(ms), 4),
+                           "tflops": round(w.flops / (avg * 1e-3) / 1e12, 1)}
+    status = attn.device_status()
+
+    # ---------------- end to end through the public API with host buffers
+    h2d = sum(sum(t.numel() * t.element_size() for t in host) for _, _, host, *_ in shapes)
+    d2h = sum(o.numel() * o.element_size() + lse.numel() * 4 for *_, o, lse in shapes)
+    e2e_steps = max(2, min(args.steps, 10))
+    for w, _, host, *_ in shapes:   # warm the pinned output buffers
+        attn.fwd(host[0], host[1], host[2], scale=w.scale)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for w, _, host, *_ in shapes:
+            o_h, lse_h = attn.fwd(host[0], host[1], host[2], scale=w.scale)
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
+    e2e_val = ws * flops / (e2e_ms * 1e-3) / 1e12
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    peak, peak_sus, peak_kind = _peaks()
+    achieved = flops / (kernel_ms_total * 1e-3) / 1e12
+    traffic = None
+    tr = [_traffic_for(w.name) for w, *_ in shapes]
+    if all(t is not None for t in tr):
+        traffic = sum(tr) / len(tr)
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        v, cores, sample, _t = oracle_sample_tflops([(w, bits) for w, bits, *_ in shapes], 12.0)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{sample} (fp64 oracle, random query rows, ~12 s total)"}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "shapes": [w.describe() for w, *_ in shapes],
+                   "per_shape": per_cfg, "l2": "inputs larger than L2 (Q+K+V = 192 MiB per shape)",
+                   "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "frac_of_peak": round(value / peak, 4), "device_status": status},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": UNIT, "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_kind": f"{peak_kind} burst bf16 (cuBLAS)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_val, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+        "gpu_launches": args.steps * len(shapes),
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,166 @@
+"""Python binding of the C ABI in include/attn_fwd.h (ctypes; marshalling only).
+
+Every step of the attention forward runs in the CUDA library; this module
+checks tensor dtypes/shapes, allocates outputs with PyTorch, passes raw
+pointers and the current CUDA stream, and maps status codes to exceptions.
+There is no fallback: if the library is missing or the device is not a
+GB300, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import threading
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_ARCH = -3
+ATTN_ERR_CUDA = -4
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class _Plan(ctypes.Structure):
+    _fields_ = [("work_items", ctypes.c_int64), ("grid", ctypes.c_int), ("threads", ctypes.c_int),
+                ("q_tiles", ctypes.c_int), ("kv_tiles", ctypes.c_int), ("kv_stages", ctypes.c_int),
+                ("smem_bytes", ctypes.c_int), ("tmem_cols", ctypes.c_int)]
+
+
+EXPORTS = ("attn_fwd", "attn_status_string", "attn_fwd_plan", "attn_fwd_work_item",
+           "attn_device_status")
+
+
+def lib_path() -> str:
+    return _build.lib_path()
+
+
+def _bind(lib):
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
+    lib.attn_fwd.restype = i32
+    lib.attn_status_string.argtypes = [i32]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_fwd_plan.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(_Plan)]
+    lib.attn_fwd_plan.restype = i32
+    lib.attn_fwd_work_item.argtypes = [i64, i32, i32, i32, ctypes.POINTER(i32),
+                                       ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    lib.attn_fwd_work_item.restype = i32
+    lib.attn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
+    lib.attn_device_status.restype = i32
+    return lib
+
+
+def library(path: str | None = None):
+    """Load (once) the CUDA library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if path is not None:
+            return _bind(ctypes.CDLL(path))
+        if _lib is None:
+            p = lib_path()
+            try:
+                _lib = _bind(ctypes.CDLL(p))
+            except OSError as e:
+                raise RuntimeError(f"attention CUDA library not loadable at {p} ({e}); "
+                                   "build it with dense_attention_forward_attn_gb300.build.build()") from e
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return library().attn_status_string(int(status)).decode()
+
+
+def plan(B: int, H: int, Sq: int, Sk: int, D: int = 128, num_sms: int = 0) -> dict:
+    p = _Plan()
+    rc = library().attn_fwd_plan(B, H, Sq, Sk, D, num_sms, ctypes.byref(p))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_plan")
+    return {f: getattr(p, f) for f, _ in _Plan._fields_}
+
+
+def work_item(item: int, B: int, H: int, Sq: int):
+    bh, qt0, nq = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    rc = library().attn_fwd_work_item(item, B, H, Sq, ctypes.byref(bh), ctypes.byref(qt0),
+                                      ctypes.byref(nq))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_work_item")
+    return bh.value, qt0.value, nq.value
+
+
+def device_status(clear: bool = False) -> int:
+    w = ctypes.c_uint(0)
+    rc = library().attn_device_status(ctypes.byref(w), 1 if clear else 0)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_device_status")
+    return int(w.value)
+
+
+def _check(t, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.dim() != 4:
+        raise TypeError(f"{name} must be a 4-D torch.bfloat16 tensor [B, H, S, D]")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous ([B, H, S, D] row-major)")
+
+
+def fwd_into(q, k, v, o, lse=None, scale: float | None = None, stream=None) -> None:
+    """Device tensors only: write softmax(scale q k^T) v into `o` (and LSE into `lse`)."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _check(t, n)
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    if tuple(k.shape) != (B, H, Sk, D) or tuple(v.shape) != (B, H, Sk, D) or tuple(o.shape) != (B, H, Sq, D):
+        raise ValueError("shape mismatch between q, k, v, o")
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Sq)
+                            or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 tensor [B, H, Sq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = library().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                            lse.data_ptr() if lse is not None else None, B, H, Sq, Sk, D,
+                            float(scale), stream)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+
+
+def fwd(q, k, v, scale: float | None = None, return_lse: bool = True):
+    """Attention forward.  q [B,H,Sq,D], k/v [B,H,Sk,D], BF16 contiguous.
+
+    CUDA tensors: runs on the current stream, returns (o, lse) on the device.
+    CPU tensors: copies the inputs to the current CUDA device (pinned host
+    memory, asynchronous), runs, copies O and LSE back and returns CPU tensors.
+    """
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n)
+    host = not q.is_cuda
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        q, k, v = (t.pin_memory().to(dev, non_blocking=True) for t in (q, k, v))
+    B, H, Sq, D = q.shape
+    o = torch.empty((B, H, Sq, D), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device) if return_lse else None
+    fwd_into(q, k, v, o, lse, scale)
+    if host:
+        o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        o_h.copy_(o, non_blocking=True)
+        lse_h = None
+        if lse is not None:
+            lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+            lse_h.copy_(lse, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return o_h, lse_h
+    return o, lse

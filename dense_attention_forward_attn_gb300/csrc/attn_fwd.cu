@@ -1,0 +1,224 @@
+// attn_fwd.cu -- host side of the C ABI declared in include/attn_fwd.h:
+// argument checks, TMA tensor-map encoding, persistent-grid sizing, launch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn_fwd.h"
+#include "attn_fwd_kernel.cuh"
+
+namespace {
+
+struct DeviceInfo {
+  bool ready = false;
+  int cc_major = 0, cc_minor = 0;
+  int num_sms = 0;
+  int smem_optin = 0;
+  bool attr_set = false;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int device_info(int dev, DeviceInfo* out) {
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    d.ready = true;
+  }
+  if (d.cc_major != 10 || d.cc_minor != 3) return ATTN_ERR_ARCH;
+  if (d.smem_optin < static_cast<int>(attn::kSmemBytes)) return ATTN_ERR_ARCH;
+  if (!d.attr_set) {
+    if (cudaFuncSetAttribute(attn::attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(attn::kSmemBytes)) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    d.attr_set = true;
+  }
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *out = d;
+  return ATTN_OK;
+}
+
+// [BH, S, 128] BF16 viewed as a 3-D tensor (128, S, BH); box 64 x 128 x 1, 128-byte swizzle.
+int encode_bhsd(CUtensorMap* map, const void* base, int64_t bh, int64_t s) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(attn::kHeadDim), static_cast<cuuint64_t>(s),
+                        static_cast<cuuint64_t>(bh)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(attn::kHeadDim) * 2,
+                           static_cast<cuuint64_t>(s) * attn::kHeadDim * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return na && nb && x < y + nb && y < x + na;
+}
+
+// Shape checks shared by attn_fwd and attn_fwd_plan.
+int check_shape(int B, int H, int Sq, int Sk, int D) {
+  if (B < 0 || H < 0 || Sq < 0 || Sk < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+  if (D != attn::kHeadDim) return ATTN_ERR_UNSUPPORTED;
+  const int64_t bh = static_cast<int64_t>(B) * H;
+  if (bh == 0 || Sq == 0) return ATTN_OK;   // empty problem
+  if (Sk == 0) return ATTN_ERR_INVALID_ARG;
+  if (Sq % attn::kBlockM != 0 || Sk % attn::kBlockN != 0) return ATTN_ERR_UNSUPPORTED;
+  const int64_t items = bh * ((Sq / attn::kBlockM + 1) / 2);
+  if (bh > INT32_MAX || items > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported shape or parameter";
+    case ATTN_ERR_ARCH: return "device is not a compute capability 10.3 (GB300) GPU";
+    case ATTN_ERR_CUDA: return "CUDA runtime or driver call failed";
+    default: return "unknown status";
+  }
+}
+
+int attn_fwd_plan(int B, int H, int Sq, int Sk, int D, int num_sms, attn_plan* plan) {
+  if (plan == nullptr) return ATTN_ERR_INVALID_ARG;
+  const int rc = check_shape(B, H, Sq, Sk, D);
+  if (rc != ATTN_OK) return rc;
+  if (num_sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+  }
+  std::memset(plan, 0, sizeof(*plan));
+  const int64_t bh = static_cast<int64_t>(B) * H;
+  plan->q_tiles = Sq / attn::kBlockM;
+  plan->kv_tiles = Sk / attn::kBlockN;
+  plan->work_items = (Sq == 0) ? 0 : bh * ((plan->q_tiles + 1) / 2);
+  plan->grid = static_cast<int>(plan->work_items < num_sms ? plan->work_items : num_sms);
+  plan->threads = attn::kThreads;
+  plan->kv_stages = attn::kKvStages;
+  plan->smem_bytes = static_cast<int>(attn::kSmemBytes);
+  plan->tmem_cols = static_cast<int>(attn::kTmemCols);
+  return ATTN_OK;
+}
+
+int attn_fwd_work_item(int64_t item, int B, int H, int Sq, int* bh, int* q_tile0, int* n_q_tiles) {
+  if (bh == nullptr || q_tile0 == nullptr || n_q_tiles == nullptr) return ATTN_ERR_INVALID_ARG;
+  const int rc = check_shape(B, H, Sq, attn::kBlockN, attn::kHeadDim);
+  if (rc != ATTN_OK) return rc;
+  const int q_tiles = Sq / attn::kBlockM;
+  const int pairs = (q_tiles + 1) / 2;
+  const int64_t items = static_cast<int64_t>(B) * H * pairs;
+  if (item < 0 || item >= items) return ATTN_ERR_INVALID_ARG;
+  const attn::WorkItem w = attn::decode_item(static_cast<int>(item), pairs, q_tiles);
+  *bh = w.bh;
+  *q_tile0 = w.qt0;
+  *n_q_tiles = w.has_q1 ? 2 : 1;
+  return ATTN_OK;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int Sq, int Sk, int D, float scale, void* stream) {
+  int rc = check_shape(B, H, Sq, Sk, D);
+  if (rc != ATTN_OK) return rc;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (scale < 0.f) return ATTN_ERR_UNSUPPORTED;
+  const int64_t bh = static_cast<int64_t>(B) * H;
+  if (bh == 0 || Sq == 0) return ATTN_OK;
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  auto mis16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+  if (mis16(q) || mis16(k) || mis16(v) || mis16(o)) return ATTN_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+  const size_t nq = static_cast<size_t>(bh) * Sq * D * 2, nk = static_cast<size_t>(bh) * Sk * D * 2;
+  const size_t nl = lse ? static_cast<size_t>(bh) * Sq * 4 : 0;
+  if (overlaps(o, nq, q, nq) || overlaps(o, nq, k, nk) || overlaps(o, nq, v, nk) ||
+      overlaps(lse, nl, q, nq) || overlaps(lse, nl, k, nk) || overlaps(lse, nl, v, nk) ||
+      overlaps(lse, nl, o, nq))
+    return ATTN_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  DeviceInfo info;
+  rc = device_info(dev, &info);
+  if (rc != ATTN_OK) return rc;
+
+  alignas(64) CUtensorMap tm_q, tm_k, tm_v;
+  if (encode_bhsd(&tm_q, q, bh, Sq) != ATTN_OK || encode_bhsd(&tm_k, k, bh, Sk) != ATTN_OK ||
+      encode_bhsd(&tm_v, v, bh, Sk) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+
+  attn::Params p;
+  p.o = o;
+  p.lse = lse;
+  p.sq = Sq;
+  p.q_tiles = Sq / attn::kBlockM;
+  p.kv_tiles = Sk / attn::kBlockN;
+  p.pairs_per_head = (p.q_tiles + 1) / 2;
+  p.num_items = static_cast<int>(bh * p.pairs_per_head);
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  const int grid = p.num_items < info.num_sms ? p.num_items : info.num_sms;
+
+  attn::attn_fwd_kernel<<<grid, attn::kThreads, attn::kSmemBytes,
+                          static_cast<cudaStream_t>(stream)>>>(tm_q, tm_k, tm_v, p);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+int attn_device_status(unsigned int* word, int clear) {
+  if (word == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (cudaMemcpyFromSymbol(word, attn::g_attn_status, sizeof(unsigned int)) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  if (clear) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(attn::g_attn_status, &zero, sizeof(unsigned int)) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+  }
+  return ATTN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,613 @@
+// attn_fwd_kernel.cuh -- the dense, non-causal, BF16, head_dim-128 attention
+// forward for sm_103a: O = softmax(scale * Q K^T) V and the natural-log LSE.
+//
+// Design (from "B200 Attention Kernel from Scratch to Near-SOTA in 60 Diagrams",
+// re-targeted to GB300):
+//   * Chapter 1 / 5: a work item is (batch*head, a pair of 128-row Q tiles); the
+//     KV loop over 128-row K/V tiles runs inside the CTA; each Q tile keeps its
+//     own S/P and O in tensor memory (TMEM: S0 | S1 | O0 | O1 = 512 columns).
+//   * Chapter 2 / 10: P is written back into TMEM as packed BF16 pairs over the
+//     upper half of its S region and feeds the P*V tcgen05.mma as the A operand.
+//   * Chapter 3: Q/K/V are staged by TMA with 128-byte swizzle; Q and K are
+//     K-major operands, V is the MN-major B operand of P*V.
+//   * Chapter 4 / 5 / 12: warp roles -- two softmax warpgroups (one per Q tile),
+//     one correction warpgroup (conditional O rescale and the epilogue), one TMA
+//     warp and one MMA-issuing warp; handoffs use mbarriers only.
+//   * Chapter 6: a ring of KV_STAGES shared slots, each holding one K or one V
+//     tile; token t and t+KV_STAGES share a slot; a K token is released after
+//     the last Q tile's Q*K^T, a V token after the last Q tile's P*V.
+//   * Chapter 7: the MMA order per tile is P_qV(i) then Q_qK(i+1); the stream
+//     continues across work items (Chapter 14), so the next item's first Q*K^T
+//     is issued as soon as its Q tile and first K tile are resident.
+//   * Chapter 8: base-2 exponentials with the scale folded into log2(e), the row
+//     max taken on raw scores, ex2.approx.ftz.
+//   * Chapter 11: the kept row max is replaced only when a tile's max exceeds it
+//     by at least 8 (base-2 units); otherwise P is taken against the stale max.
+//   * Chapter 13: P*V is issued in two parts, K-steps 2..7 once P's upper 96
+//     columns are in TMEM and O is safe, K-steps 0..1 once the lower 32 are.
+//   * Chapter 14: persistent CTAs, one per SM, static stride over work items;
+//     barriers are initialised once and their phases carried across items.
+// LSE = (kept max + log2(row sum)) * ln 2 ("Attention for sm90, Line by Line",
+// the exp2 question: the residual is stored in natural-log units).
+//
+// Every mbarrier wait is bounded in time: on expiry the CTA records a status
+// bit in a device word, stops issuing work, waits for its own copies and MMAs in
+// flight, frees TMEM and exits.
+#pragma once
+#include <cuda.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+#ifndef ATTN_KV_STAGES
+#define ATTN_KV_STAGES 3
+#endif
+
+namespace attn {
+
+constexpr int kBlockM = 128;   // rows of a Q tile
+constexpr int kBlockN = 128;   // rows of a K/V tile
+constexpr int kHeadDim = 128;
+constexpr int kKvStages = ATTN_KV_STAGES;
+constexpr int kThreads = 512;
+constexpr uint32_t kTileBytes = kBlockM * kHeadDim * 2;   // 32 KiB
+constexpr uint32_t kSlabBytes = kTileBytes / 2;           // 128 rows x 64 columns (128 B rows)
+constexpr float kRebaseThresholdLog2 = 8.0f;
+
+// Warp roles.
+constexpr int kCorrWarp0 = 8;
+constexpr int kLoadWarp = 12;
+constexpr int kMmaWarp = 13;
+
+// Register split (setmaxnreg): 2 softmax WGs + correction WG + misc WG.
+// (kRegSoftmax * 2 + kRegCorr + kRegMisc) * 128 threads must equal
+// 65536 = kThreads * 128 (the registers the block is launched with).
+constexpr uint32_t kRegSoftmax = 176;
+constexpr uint32_t kRegCorr = 88;
+constexpr uint32_t kRegMisc = 72;
+static_assert((kRegSoftmax * 2 + kRegCorr + kRegMisc) * 128 == 65536, "register split");
+
+// TMEM columns.
+constexpr uint32_t kTmemCols = 512;
+__host__ __device__ constexpr uint32_t col_s(int q) { return q ? 128u : 0u; }
+__host__ __device__ constexpr uint32_t col_o(int q) { return q ? 384u : 256u; }
+constexpr uint32_t kColP = 64;   // packed P sits over S columns 64..127 of its stage
+
+// Device status bits (bounded waits that expired, by role).
+constexpr unsigned kStatusTimeoutLoad = 1u << 0;
+constexpr unsigned kStatusTimeoutMma = 1u << 1;
+constexpr unsigned kStatusTimeoutSoftmax = 1u << 2;
+constexpr unsigned kStatusTimeoutCorrection = 1u << 3;
+constexpr unsigned kStatusTimeoutDrain = 1u << 4;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
+constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s for own in-flight work
+
+struct alignas(8) SmemCtl {
+  uint64_t q_full[2], q_empty[2];
+  uint64_t kv_full[kKvStages], kv_empty[kKvStages];
+  uint64_t s_full[2];      // MMA -> softmax: S_q(i) in TMEM
+  uint64_t p_hi_full[2];   // softmax (P cols 32..127) + correction (O safe) -> MMA
+  uint64_t p_lo_full[2];   // softmax (P cols 0..31) -> MMA
+  uint64_t stats_full[2];  // softmax -> correction: per-row rescale factor published
+  uint64_t o_full[2];      // MMA -> correction: last P*V of the item done
+  uint64_t final_full[2];  // softmax -> correction: final row max / row sum published
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort_flag;
+  float alpha[2][2][kBlockM];   // [stage][tile parity][row]
+  float row_m[2][2][kBlockM];   // [stage][item parity][row], base-2 units
+  float row_l[2][2][kBlockM];   // [stage][item parity][row]
+};
+
+constexpr uint32_t kCtlOffset = (2 + kKvStages) * kTileBytes;
+constexpr uint32_t kSmemBytes = kCtlOffset + sizeof(SmemCtl) + 1024;   // +1 KiB for alignment
+
+struct Params {
+  void* o;          // BF16 [BH, Sq, 128]
+  float* lse;       // fp32 [BH, Sq] or null
+  int sq;
+  int q_tiles;      // Sq / 128
+  int kv_tiles;     // Sk / 128
+  int pairs_per_head;
+  int num_items;
+  float scale_log2; // scale * log2(e)
+};
+
+struct WorkItem {
+  int bh;       // flattened batch*head
+  int qt0;      // first Q tile of the pair
+  bool has_q1;  // second Q tile exists (false for the last pair of an odd tile count)
+};
+
+// Work item -> (bh, Q-tile pair); consecutive items walk the Q pairs of one head.
+__host__ __device__ inline WorkItem decode_item(int item, int pairs_per_head, int q_tiles) {
+  WorkItem w;
+  w.bh = item / pairs_per_head;
+  const int pair = item - w.bh * pairs_per_head;
+  w.qt0 = 2 * pair;
+  w.has_q1 = (w.qt0 + 1) < q_tiles;
+  return w;
+}
+
+// tcgen05 shared-memory matrix descriptor, 128-byte swizzle.
+//   bits  0-13  start address >> 4      bits 16-29  leading byte offset >> 4
+//   bits 32-45  stride byte offset >> 4 bits 46-48  fixed 0b001
+//   bits 49-51  base offset (0: tiles are 1024-byte aligned)
+//   bits 61-63  swizzle mode (2 = 128-byte)
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor, .kind::f16 with BF16 A/B and FP32 accumulate.
+//   bits 4-5 D format (1 = F32), 7-9 A format (1 = BF16), 10-12 B format (1 = BF16),
+//   bit 15 A major (0 = K), bit 16 B major (1 = MN), bits 17-22 N >> 3, bits 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t make_idesc_bf16(uint32_t m, uint32_t n, uint32_t b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major << 16) | ((n >> 3) << 17) |
+         ((m >> 4) << 24);
+}
+
+__device__ unsigned int g_attn_status = 0;
+
+struct Ctx {
+  SmemCtl* ctl;
+  uint32_t smem_base;   // 1024-aligned shared address of Q0
+  uint32_t tmem;        // TMEM base address
+  uint32_t warp;
+  uint32_t lane;
+
+  __device__ uint32_t bar(const uint64_t& b) const { return ptx::smem_u32(&b); }
+  __device__ uint32_t sq(int q) const { return smem_base + q * kTileBytes; }
+  __device__ uint32_t skv(int s) const { return smem_base + (2 + s) * kTileBytes; }
+
+  // Warp-uniform bounded wait; all 32 lanes call it.  false = timed out or aborted.
+  __device__ bool wait(const uint64_t& b, uint32_t parity, unsigned role_bit) const {
+    const uint32_t addr = bar(b);
+    if (__all_sync(0xffffffffu, ptx::mbar_try_wait(addr, parity))) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (true) {
+      if (__all_sync(0xffffffffu, ptx::mbar_try_wait(addr, parity))) return true;
+      const bool stop = ctl->abort_flag != 0 || (ptx::globaltimer_ns() - t0) > kWaitLimitNs;
+      if (__any_sync(0xffffffffu, stop)) {
+        if (lane == 0) {
+          ctl->abort_flag = 1;
+          atomicOr(&g_attn_status, role_bit);
+        }
+        __syncwarp();
+        return false;
+      }
+    }
+  }
+
+  // Bounded wait on this warp's own in-flight work, ignoring the abort flag.
+  __device__ void drain_wait(const uint64_t& b, uint32_t parity) const {
+    const uint32_t addr = bar(b);
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!__all_sync(0xffffffffu, ptx::mbar_try_wait(addr, parity))) {
+      if (__any_sync(0xffffffffu, (ptx::globaltimer_ns() - t0) > kDrainLimitNs)) {
+        if (lane == 0) atomicOr(&g_attn_status, kStatusTimeoutDrain);
+        return;
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------------ TMA warp
+__device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const CUtensorMap* tm_q,
+                                          const CUtensorMap* tm_k, const CUtensorMap* tm_v) {
+  SmemCtl* ctl = c.ctl;
+  int slot = 0;
+  uint32_t phase = 0;          // phase of the kv ring round being filled
+  uint32_t kv_used = 0;        // bit s: slot s received a load
+  uint32_t kv_last_par = 0;    // bit s: phase parity of the last load into slot s
+  uint32_t q_cnt[2] = {0, 0};  // Q loads issued per stage
+  bool ok = true;
+
+  auto load_kv = [&](const CUtensorMap* tm, int bh, int row) -> bool {
+    if (!c.wait(ctl->kv_empty[slot], phase ^ 1u, kStatusTimeoutLoad)) return false;
+    if (c.lane == 0) {
+      const uint32_t fb = c.bar(ctl->kv_full[slot]);
+      ptx::mbar_arrive_expect_tx(fb, kTileBytes);
+      ptx::tma_load_3d(c.skv(slot), tm, fb, 0, row, bh);
+      ptx::tma_load_3d(c.skv(slot) + kSlabBytes, tm, fb, 64, row, bh);
+    }
+    __syncwarp();
+    kv_used |= 1u << slot;
+    kv_last_par = (kv_last_par & ~(1u << slot)) | (phase << slot);
+    if (++slot == kKvStages) { slot = 0; phase ^= 1u; }
+    return true;
+  };
+  auto load_q = [&](int q, int bh, int row) -> bool {
+    if (!c.wait(ctl->q_empty[q], (q_cnt[q] & 1u) ^ 1u, kStatusTimeoutLoad)) return false;
+    if (c.lane == 0) {
+      const uint32_t fb = c.bar(ctl->q_full[q]);
+      ptx::mbar_arrive_expect_tx(fb, kTileBytes);
+      ptx::tma_load_3d(c.sq(q), tm_q, fb, 0, row, bh);
+      ptx::tma_load_3d(c.sq(q) + kSlabBytes, tm_q, fb, 64, row, bh);
+    }
+    __syncwarp();
+    ++q_cnt[q];
+    return true;
+  };
+
+  for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
+    const WorkItem w = decode_item(item, p.pairs_per_head, p.q_tiles);
+    const int row0 = w.qt0 * kBlockM;
+    ok = load_q(0, w.bh, row0) && load_kv(tm_k, w.bh, 0);
+    if (ok && w.has_q1) ok = load_q(1, w.bh, row0 + kBlockM);
+    if (ok) ok = load_kv(tm_v, w.bh, 0);
+    for (int j = 1; ok && j < p.kv_tiles; ++j)
+      ok = load_kv(tm_k, w.bh, j * kBlockN) && load_kv(tm_v, w.bh, j * kBlockN);
+  }
+  if (!ok) {
+    // Stop issuing; wait for the copies this warp already started.
+    for (int s = 0; s < kKvStages; ++s)
+      if ((kv_used >> s) & 1u) c.drain_wait(ctl->kv_full[s], (kv_last_par >> s) & 1u);
+    for (int q = 0; q < 2; ++q)
+      if (q_cnt[q]) c.drain_wait(ctl->q_full[q], (q_cnt[q] - 1) & 1u);
+  }
+}
+
+// ------------------------------------------------------------------ MMA warp
+__device__ __forceinline__ void issue_qk(const Ctx& c, int q, int kslot) {
+  constexpr uint32_t idesc = make_idesc_bf16(128, 128, 0);
+  const uint32_t d = c.tmem + col_s(q);
+#pragma unroll
+  for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * kSlabBytes + (kk & 3) * 32;
+    const uint64_t a = smem_desc_sw128(c.sq(q) + off, 16, 1024);
+    const uint64_t b = smem_desc_sw128(c.skv(kslot) + off, 16, 1024);
+    ptx::mma_ss(d, a, b, idesc, kk > 0);
+  }
+}
+
+// K-steps [k0, k1) of P_q * V: A = packed P in TMEM, B = V tile (MN-major, 128B swizzle).
+__device__ __forceinline__ void issue_pv(const Ctx& c, int q, int vslot, int k0, int k1,
+                                         bool overwrite_first) {
+  constexpr uint32_t idesc = make_idesc_bf16(128, 128, 1);
+  const uint32_t d = c.tmem + col_o(q);
+  const uint32_t a0 = c.tmem + col_s(q) + kColP;
+  for (int kk = k0; kk < k1; ++kk) {
+    const uint64_t b = smem_desc_sw128(c.skv(vslot) + kk * 16 * 128, kSlabBytes, 1024);
+    ptx::mma_ts(d, a0 + kk * 8, b, idesc, !(overwrite_first && kk == k0));
+  }
+}
+
+__device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
+  SmemCtl* ctl = c.ctl;
+  const bool leader = c.lane == 0;
+  int slot = 0;
+  uint32_t phase = 0;
+  uint32_t q_cnt[2] = {0, 0};
+  uint32_t pv_phase[2] = {0, 0};
+  bool ok = true;
+
+  auto next_kv = [&](int& s_out) -> bool {
+    s_out = slot;
+    const bool r = c.wait(ctl->kv_full[slot], phase, kStatusTimeoutMma);
+    if (++slot == kKvStages) { slot = 0; phase ^= 1u; }
+    return r;
+  };
+  // Q_qK(j): Q_q of the current item against the K tile in kslot.
+  auto qk = [&](int q, int kslot, bool new_item, bool last_qk, bool release_k) -> bool {
+    if (new_item) {
+      if (!c.wait(ctl->q_full[q], q_cnt[q] & 1u, kStatusTimeoutMma)) return false;
+      ++q_cnt[q];
+    }
+    ptx::tc_fence_after();
+    if (leader) {
+      issue_qk(c, q, kslot);
+      ptx::mma_commit(c.bar(ctl->s_full[q]));
+      if (last_qk) ptx::mma_commit(c.bar(ctl->q_empty[q]));
+      if (release_k) ptx::mma_commit(c.bar(ctl->kv_empty[kslot]));
+    }
+    __syncwarp();
+    return true;
+  };
+  auto pv = [&](int q, int vslot, bool first_tile) -> bool {
+    if (!c.wait(ctl->p_hi_full[q], pv_phase[q], kStatusTimeoutMma)) return false;
+    ptx::tc_fence_after();
+    if (leader) issue_pv(c, q, vslot, 2, 8, first_tile);
+    __syncwarp();
+    if (!c.wait(ctl->p_lo_full[q], pv_phase[q], kStatusTimeoutMma)) return false;
+    ptx::tc_fence_after();
+    if (leader) issue_pv(c, q, vslot, 0, 2, false);
+    __syncwarp();
+    pv_phase[q] ^= 1u;
+    return true;
+  };
+
+  int item = blockIdx.x;
+  if (item < p.num_items) {
+    WorkItem w = decode_item(item, p.pairs_per_head, p.q_tiles);
+    int j = 0;
+    int kslot;
+    const bool one_tile = p.kv_tiles == 1;
+    ok = next_kv(kslot) && qk(0, kslot, true, one_tile, !w.has_q1);
+    if (ok && w.has_q1) ok = qk(1, kslot, true, one_tile, true);
+    while (ok) {
+      int vslot;
+      if (!(ok = next_kv(vslot))) break;
+      const bool last_of_item = j == p.kv_tiles - 1;
+      int nitem = item, nj = j + 1;
+      if (last_of_item) { nitem = item + gridDim.x; nj = 0; }
+      const bool has_next = nitem < p.num_items;
+      const WorkItem nw = last_of_item ? (has_next ? decode_item(nitem, p.pairs_per_head, p.q_tiles) : w) : w;
+      const bool next_last_qk = nj == p.kv_tiles - 1;
+
+      // stage 0: P0 V(j), then Q0 K(next)
+      if (!(ok = pv(0, vslot, j == 0))) break;
+      if (leader) {
+        if (last_of_item) ptx::mma_commit(c.bar(ctl->o_full[0]));
+        if (!w.has_q1) ptx::mma_commit(c.bar(ctl->kv_empty[vslot]));
+      }
+      __syncwarp();
+      int nkslot = 0;
+      if (has_next) {
+        if (!(ok = next_kv(nkslot))) break;
+        if (!(ok = qk(0, nkslot, nj == 0, next_last_qk, !nw.has_q1))) break;
+      }
+      // stage 1: P1 V(j), then Q1 K(next)
+      if (w.has_q1) {
+        if (!(ok = pv(1, vslot, j == 0))) break;
+        if (leader) {
+          if (last_of_item) ptx::mma_commit(c.bar(ctl->o_full[1]));
+          ptx::mma_commit(c.bar(ctl->kv_empty[vslot]));
+        }
+        __syncwarp();
+      }
+      if (has_next && nw.has_q1)
+        if (!(ok = qk(1, nkslot, nj == 0, next_last_qk, true))) break;
+      if (!has_next) break;
+      item = nitem;
+      j = nj;
+      w = nw;
+    }
+  }
+  // Wait for every MMA this thread issued before TMEM can be released.
+  if (leader) ptx::mma_commit(c.bar(ctl->drain));
+  __syncwarp();
+  c.drain_wait(ctl->drain, 0);
+}
+
+// ------------------------------------------------------------------ softmax warpgroups
+__device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int q) {
+  SmemCtl* ctl = c.ctl;
+  const uint32_t row_base = 32u * (c.warp & 3u);
+  const int row = static_cast<int>(row_base + c.lane);
+  const uint32_t taddr_s = c.tmem + (row_base << 16) + col_s(q);
+  const float scale_log2 = p.scale_log2;
+  uint32_t tphase = 0;
+  uint32_t items_q = 0;
+
+  for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+    const WorkItem w = decode_item(item, p.pairs_per_head, p.q_tiles);
+    if (q == 1 && !w.has_q1) continue;
+    float m_kept = 0.f;   // base-2 units; set on the first tile
+    float l = 0.f;
+    for (int j = 0; j < p.kv_tiles; ++j) {
+      if (!c.wait(ctl->s_full[q], tphase, kStatusTimeoutSoftmax)) return;
+      ptx::tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) ptx::tmem_ld_32x32b_x32(taddr_s + 32 * cc, sr[cc]);
+      ptx::tmem_wait_ld();
+
+      // Row max over the raw scores: four independent chains.
+      float mx[4];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        float m = __uint_as_float(sr[cc][0]);
+#pragma unroll
+        for (int i = 1; i < 31; i += 2)
+          m = ptx::fmax3(m, __uint_as_float(sr[cc][i]), __uint_as_float(sr[cc][i + 1]));
+        mx[cc] = fmaxf(m, __uint_as_float(sr[cc][31]));
+      }
+      const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
+      float alpha = 1.f;
+      if (j == 0) {
+        m_kept = m_tile;
+      } else if (m_tile - m_kept >= kRebaseThresholdLog2) {
+        alpha = ptx::ex2_ftz(m_kept - m_tile);
+        l *= alpha;
+        m_kept = m_tile;
+      }
+      ctl->alpha[q][tphase][row] = alpha;
+      ptx::mbar_arrive(c.bar(ctl->stats_full[q]));
+
+      const float neg_m = -m_kept;
+      float sum[4];
+      // Upper 96 columns first (packed P columns 16..63), then publish them.
+#pragma unroll
+      for (int cc = 3; cc >= 0; --cc) {
+        uint32_t pk[16];
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ptx::ex2_ftz(fmaf(__uint_as_float(sr[cc][2 * i]), scale_log2, neg_m));
+          const float p1 = ptx::ex2_ftz(fmaf(__uint_as_float(sr[cc][2 * i + 1]), scale_log2, neg_m));
+          s0 += p0;
+          s1 += p1;
+          pk[i] = ptx::pack_bf16x2(p0, p1);
+        }
+        sum[cc] = s0 + s1;
+        ptx::tmem_st_32x32b_x16(taddr_s + kColP + 16 * cc, pk);
+        if (cc == 1) {
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(c.bar(ctl->p_hi_full[q]));
+        }
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(c.bar(ctl->p_lo_full[q]));
+      l += (sum[3] + sum[2]) + (sum[1] + sum[0]);
+      tphase ^= 1u;
+    }
+    ctl->row_m[q][items_q & 1u][row] = m_kept;
+    ctl->row_l[q][items_q & 1u][row] = l;
+    ptx::mbar_arrive(c.bar(ctl->final_full[q]));
+    ++items_q;
+  }
+}
+
+// ------------------------------------------------------------------ correction warpgroup
+__device__ __forceinline__ bool epilogue(const Ctx& c, const Params& p, int q, const WorkItem& w,
+                                         uint32_t idx) {
+  SmemCtl* ctl = c.ctl;
+  if (!c.wait(ctl->final_full[q], idx & 1u, kStatusTimeoutCorrection)) return false;
+  if (!c.wait(ctl->o_full[q], idx & 1u, kStatusTimeoutCorrection)) return false;
+  ptx::tc_fence_after();
+  const uint32_t row_base = 32u * (c.warp & 3u);
+  const int row = static_cast<int>(row_base + c.lane);
+  const float m = ctl->row_m[q][idx & 1u][row];
+  const float l = ctl->row_l[q][idx & 1u][row];
+  const float inv_l = 1.0f / l;
+  const int grow = (w.qt0 + q) * kBlockM + row;
+  uint8_t* out = static_cast<uint8_t*>(p.o) + (static_cast<size_t>(w.bh) * p.sq + grow) * (kHeadDim * 2);
+  const uint32_t taddr_o = c.tmem + (row_base << 16) + col_o(q);
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    uint32_t r[32];
+    ptx::tmem_ld_32x32b_x32(taddr_o + 32 * cc, r);
+    ptx::tmem_wait_ld();
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+      ptx::st_global_v4(out + cc * 64 + v * 16, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+  }
+  if (p.lse != nullptr)
+    p.lse[static_cast<size_t>(w.bh) * p.sq + grow] = (m + log2f(l)) * 0.69314718055994530942f;
+  ptx::tc_fence_before();
+  return true;
+}
+
+__device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
+  SmemCtl* ctl = c.ctl;
+  const uint32_t row_base = 32u * (c.warp & 3u);
+  const int row = static_cast<int>(row_base + c.lane);
+  uint32_t tphase[2] = {0, 0};
+  uint32_t items_done[2] = {0, 0};
+  bool pending[2] = {false, false};
+  WorkItem pend_w[2];
+
+  for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
+    const WorkItem w = decode_item(item, p.pairs_per_head, p.q_tiles);
+    for (int j = 0; j < p.kv_tiles; ++j) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        if (q == 1 && !w.has_q1) continue;
+        if (j == 0 && pending[q]) {
+          if (!epilogue(c, p, q, pend_w[q], items_done[q])) return;
+          ++items_done[q];
+          pending[q] = false;
+        }
+        if (!c.wait(ctl->stats_full[q], tphase[q], kStatusTimeoutCorrection)) return;
+        const float a = ctl->alpha[q][tphase[q]][row];
+        if (__any_sync(0xffffffffu, a != 1.0f)) {
+          const uint32_t taddr_o = c.tmem + (row_base << 16) + col_o(q);
+          ptx::tc_fence_after();
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(taddr_o + 32 * cc, r);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
+            ptx::tmem_st_32x32b_x32(taddr_o + 32 * cc, r);
+          }
+          ptx::tmem_wait_st();
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(c.bar(ctl->p_hi_full[q]));
+        tphase[q] ^= 1u;
+      }
+    }
+    pending[0] = true;
+    pend_w[0] = w;
+    if (w.has_q1) {
+      pending[1] = true;
+      pend_w[1] = w;
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+    if (pending[q] && !epilogue(c, p, q, pend_w[q], items_done[q])) return;
+}
+
+// ------------------------------------------------------------------ kernel
+__global__ void __launch_bounds__(kThreads, 1)
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  Ctx c;
+  c.smem_base = base;
+  c.ctl = reinterpret_cast<SmemCtl*>(smem_raw + (base - raw) + kCtlOffset);
+  c.warp = threadIdx.x >> 5;
+  c.lane = threadIdx.x & 31u;
+  SmemCtl* ctl = c.ctl;
+
+  if (threadIdx.x == 0) {
+    for (int q = 0; q < 2; ++q) {
+      ptx::mbar_init(c.bar(ctl->q_full[q]), 1);
+      ptx::mbar_init(c.bar(ctl->q_empty[q]), 1);
+      ptx::mbar_init(c.bar(ctl->s_full[q]), 1);
+      ptx::mbar_init(c.bar(ctl->p_hi_full[q]), 2 * 128);   // softmax rows + correction rows
+      ptx::mbar_init(c.bar(ctl->p_lo_full[q]), 128);
+      ptx::mbar_init(c.bar(ctl->stats_full[q]), 128);
+      ptx::mbar_init(c.bar(ctl->o_full[q]), 1);
+      ptx::mbar_init(c.bar(ctl->final_full[q]), 128);
+    }
+    for (int s = 0; s < kKvStages; ++s) {
+      ptx::mbar_init(c.bar(ctl->kv_full[s]), 1);
+      ptx::mbar_init(c.bar(ctl->kv_empty[s]), 1);
+    }
+    ptx::mbar_init(c.bar(ctl->drain), 1);
+    ctl->abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (c.warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(&ctl->tmem_base), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (c.warp == kLoadWarp && c.lane == 0) {
+    ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  c.tmem = ctl->tmem_base;
+
+  if (c.warp < kCorrWarp0) {
+    ptx::setmaxnreg_inc<kRegSoftmax>();
+    softmax_role(c, p, static_cast<int>(c.warp >> 2));
+  } else if (c.warp < kLoadWarp) {
+    ptx::setmaxnreg_dec<kRegCorr>();
+    correction_role(c, p);
+  } else {
+    ptx::setmaxnreg_dec<kRegMisc>();
+    if (c.warp == kLoadWarp) load_role(c, p, &tm_q, &tm_k, &tm_v);
+    else if (c.warp == kMmaWarp) mma_role(c, p);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (c.warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(c.tmem, kTmemCols);
+  }
+}
+
+}  // namespace attn

@@ -1,0 +1,117 @@
+/*
+ * attn_fwd.h -- C ABI of the GB300 (sm_103a) dense attention forward.
+ *
+ * One operation: the dense, non-causal attention forward with head_dim 128,
+ *     O   = softmax(scale * Q K^T) V
+ *     LSE = log(sum_j exp(scale * q_i . k_j))        (natural log, per query row)
+ * computed tile by tile with the online-softmax state (running row max, row
+ * sum, unnormalised O) so the Sq x Sk score matrix never reaches memory.
+ *
+ * Where the operation is defined:
+ *   "B200 Attention Kernel from Scratch to Near-SOTA in 60 Diagrams" -- scope
+ *   (dense, head dim 128, non-causal, BF16), Chapter 1 section ii (Q, K, V and
+ *   the output share the shape [B, num_heads, seq_len, head_dim]; 128x128
+ *   tiles), Chapter 1 section B (the online-softmax update and the final
+ *   division by the row sum), Chapter 8 (base-2 exponent with the scale folded
+ *   in), Chapter 11 (the kept max is rebased only past a threshold), and the
+ *   Appendix "Benchmark Calibration" (contiguous BHLD inputs).
+ *   "Attention for sm90, Line by Line", the exp2 question: the residual LSE is
+ *   stored in natural-log units.
+ *
+ * No function here allocates device memory, copies between host and device or
+ * synchronises, unless its comment says so.  All entry points are thread-safe.
+ */
+#ifndef ATTN_FWD_H_
+#define ATTN_FWD_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+typedef enum attn_status {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = -1, /* null/misaligned pointer, negative size, aliasing, bad scale */
+  ATTN_ERR_UNSUPPORTED = -2, /* valid request outside what this build supports (D != 128, ...) */
+  ATTN_ERR_ARCH = -3,        /* the current device is not a compute capability 10.3 GPU */
+  ATTN_ERR_CUDA = -4         /* a CUDA runtime/driver call failed (launch, tensor-map encode) */
+} attn_status;
+
+/*
+ * attn_fwd -- enqueue one attention forward on `stream`.
+ *
+ *   q    device, BF16, [B, H, Sq, D] contiguous (row-major, D fastest), read only
+ *   k    device, BF16, [B, H, Sk, D] contiguous, read only
+ *   v    device, BF16, [B, H, Sk, D] contiguous, read only
+ *   o    device, BF16, [B, H, Sq, D] contiguous, written (every element)
+ *   lse  device, fp32, [B, H, Sq] contiguous, written; may be NULL (not stored)
+ *   B, H, Sq, Sk, D   sizes; supported: D == 128, Sq and Sk multiples of 128
+ *   scale             multiplies Q K^T before the softmax; finite and >= 0
+ *                     (the row max is taken on raw scores and then scaled)
+ *   stream            a cudaStream_t (NULL = the legacy default stream)
+ *
+ * Ownership: the caller owns every buffer; the library keeps no pointer after
+ * the call returns.  q, k, v, o and lse must be distinct, non-overlapping
+ * device allocations of the current device; q, k, v, o 16-byte aligned, lse
+ * 4-byte aligned.
+ *
+ * Errors: arguments are checked on the host before anything is enqueued; any
+ * error returns without launching.  B*H == 0 or Sq == 0 is a valid empty
+ * problem: ATTN_OK, nothing launched.  Sk == 0 with Sq > 0 is ATTN_ERR_INVALID_ARG
+ * (a softmax over no keys).  Sq or Sk not a multiple of 128, or D != 128, is
+ * ATTN_ERR_UNSUPPORTED.  A device that is not compute capability 10.3 gives
+ * ATTN_ERR_ARCH.  A failed launch gives ATTN_ERR_CUDA (the sticky-free launch
+ * error is cleared).  Non-finite inputs give unspecified outputs.
+ *
+ * Asynchronous: returns once the kernel is enqueued.  Results are ready when
+ * the stream reaches that point.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int Sq, int Sk, int D, float scale, void* stream);
+
+/* Static text for a status code (never NULL). */
+const char* attn_status_string(int status);
+
+/*
+ * attn_fwd_plan -- the launch attn_fwd would make, computed on the host only
+ * (no CUDA call when num_sms > 0; num_sms <= 0 queries the current device).
+ * Same argument checks as attn_fwd for the sizes.  Work decomposition:
+ * "B200 Attention Kernel from Scratch to Near-SOTA in 60 Diagrams", Chapter 5
+ * (two 128-row Q tiles per work item) and Chapter 14 (one persistent CTA per
+ * SM, work_id += gridDim.x).
+ */
+typedef struct attn_plan {
+  int64_t work_items;  /* B*H*ceil(Sq/256): (batch*head, pair of Q tiles) */
+  int grid;            /* persistent CTAs = min(num_sms, work_items) */
+  int threads;         /* threads per CTA */
+  int q_tiles;         /* Sq / 128 per head */
+  int kv_tiles;        /* Sk / 128: KV-loop iterations per work item */
+  int kv_stages;       /* shared-memory K/V ring slots */
+  int smem_bytes;      /* dynamic shared memory per CTA */
+  int tmem_cols;       /* tensor-memory columns per CTA */
+} attn_plan;
+
+int attn_fwd_plan(int B, int H, int Sq, int Sk, int D, int num_sms, attn_plan* plan);
+
+/*
+ * attn_fwd_work_item -- which (flattened batch*head, first Q tile, Q-tile
+ * count) a work item covers; the same decoding the kernel uses.  Host only.
+ */
+int attn_fwd_work_item(int64_t item, int B, int H, int Sq, int* bh, int* q_tile0, int* n_q_tiles);
+
+/*
+ * attn_device_status -- read (and with clear != 0, reset) the current device's
+ * status word.  Bit 0..3: a bounded wait inside the kernel expired (TMA,
+ * MMA, softmax, correction role); bit 4: a drain of in-flight work expired.
+ * Zero means no kernel since the last reset hit a wait limit.  Synchronous:
+ * copies 4 bytes from the device (waits for prior work on the legacy stream).
+ */
+int attn_device_status(unsigned int* word, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_FWD_H_ */

@@ -1,0 +1,183 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Tolerances (the stated bar): O max-abs <= 2e-2 and mean-abs <= 2e-3 over the
+compared elements; LSE max-abs <= 1e-3.  Small shapes are compared element by
+element over every output; the full-size workloads, in the exact launch
+configuration the benchmark times, are compared on sampled rows that the
+oracle computes one by one (first/last rows of Q tiles, every work item that
+is the last of its CTA, random rows).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_attention_forward_attn_gb300 import attn, workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+O_MAX, O_MEAN, LSE_MAX = 2e-2, 2e-3, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _status_clean():
+    torch.cuda.set_device(0)
+    attn.device_status(clear=True)
+    yield
+    torch.cuda.synchronize()
+    assert attn.device_status() == 0, "a bounded wait expired inside the kernel"
+
+
+def _run(qb, kb, vb, scale):
+    q, k, v = (wl.bits_to_torch(x).cuda() for x in (qb, kb, vb))
+    o, lse = attn.fwd(q, k, v, scale=scale)
+    torch.cuda.synchronize()
+    return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def _assert_close(o, o_ref, lse, lse_ref):
+    err = np.abs(o - o_ref)
+    lerr = np.abs(lse - lse_ref)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    assert err.max() <= O_MAX, f"O max-abs {err.max():.4g}"
+    assert err.mean() <= O_MEAN, f"O mean-abs {err.mean():.4g}"
+    assert lerr.max() <= LSE_MAX, f"LSE max-abs {lerr.max():.4g}"
+
+
+def _full_check(B, H, Sq, Sk, seed=0, scale=None, **kw):
+    qb, kb, vb = wl.make_inputs_bits(B, H, Sq, Sk, 128, seed=seed, **kw)
+    scale = 1.0 / math.sqrt(128) if scale is None else scale
+    o, lse = _run(qb, kb, vb, scale)
+    o_ref, lse_ref = oracle.attn_fwd(qb, kb, vb, scale)
+    _assert_close(o, o_ref, lse, lse_ref)
+    return o, lse
+
+
+@pytest.mark.parametrize("seed", wl.TINY.seeds)
+def test_tiny(seed):
+    w = wl.TINY
+    _full_check(w.B, w.H, w.Sq, w.Sk, seed=seed)
+
+
+def test_softmax_stress():
+    w = wl.STRESS
+    _full_check(w.B, w.H, w.Sq, w.Sk, seed=w.seeds[0], qk_std=w.qk_std,
+                spike_every=w.spike_every, spike_factor=w.spike_factor)
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 1, 128, 128),    # one Q tile (the work item's second tile idles), one KV tile
+    (1, 3, 384, 640),    # odd Q-tile count, Sq != Sk
+    (2, 2, 640, 256),    # Sq > Sk, odd tile count, two heads per batch
+    (1, 2, 256, 1152),   # many KV tiles: the 3-slot ring wraps several times
+    (3, 5, 256, 128),    # 15 work items with a single KV tile each
+])
+def test_shapes(shape):
+    _full_check(*shape, seed=sum(shape))
+
+
+def test_persistent_loop_over_many_items():
+    # 2*100*2 = 400 work items on <= 152 CTAs: every CTA runs 2-3 items and
+    # carries barrier phases, the KV ring position and the epilogue across them.
+    B, H, Sq, Sk = 2, 100, 512, 384
+    qb, kb, vb = wl.make_inputs_bits(B, H, Sq, Sk, 128, seed=21)
+    scale = 1.0 / math.sqrt(128)
+    o, lse = _run(qb, kb, vb, scale)
+    rng = np.random.Generator(np.random.PCG64(5))
+    bh = rng.integers(0, B * H, 3000)
+    rows = rng.integers(0, Sq, 3000)
+    o_ref, lse_ref = oracle.attn_fwd_rows(qb, kb, vb, scale, bh, rows)
+    _assert_close(o.reshape(B * H, Sq, 128)[bh, rows], o_ref, lse.reshape(B * H, Sq)[bh, rows], lse_ref)
+
+
+def test_zero_scale_is_uniform_average():
+    qb, kb, vb = wl.make_inputs_bits(1, 2, 256, 384, 128, seed=3)
+    o, lse = _run(qb, kb, vb, 0.0)
+    v = wl.bf16_bits_to_f32(vb).astype(np.float64)
+    mean = np.broadcast_to(v.mean(axis=2, keepdims=True), o.shape)
+    assert np.abs(o - mean).max() <= O_MAX
+    assert np.abs(lse - math.log(384)).max() <= LSE_MAX
+
+
+def test_dominant_key_copies_its_value_row():
+    B, H, Sq, Sk = 1, 1, 256, 512
+    qb, kb, vb = wl.make_inputs_bits(B, H, Sq, Sk, 128, seed=4)
+    k = wl.bf16_bits_to_f32(kb).copy()
+    k[0, 0, 300] = 4.0 * np.sign(wl.bf16_bits_to_f32(qb)[0, 0, 0] + 1e-3)   # aligned with q row 0
+    kb = wl.to_bf16_bits(k)
+    o, lse = _run(qb, kb, vb, 1.0)
+    o_ref, lse_ref = oracle.attn_fwd(qb, kb, vb, 1.0)
+    _assert_close(o, o_ref, lse, lse_ref)
+    v = wl.bf16_bits_to_f32(vb)
+    assert np.abs(o[0, 0, 0] - v[0, 0, 300]).max() <= O_MAX
+
+
+def test_run_to_run_bitwise_deterministic():
+    qb, kb, vb = wl.make_inputs_bits(2, 8, 1024, 1024, 128, seed=8)
+    q, k, v = (wl.bits_to_torch(x).cuda() for x in (qb, kb, vb))
+    o1, l1 = attn.fwd(q, k, v)
+    o2, l2 = attn.fwd(q, k, v)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_lse_optional_and_host_buffers():
+    qb, kb, vb = wl.make_inputs_bits(1, 2, 256, 256, 128, seed=9)
+    q, k, v = (wl.bits_to_torch(x) for x in (qb, kb, vb))
+    o_dev, lse_dev = attn.fwd(q.cuda(), k.cuda(), v.cuda())
+    o_nolse, none = attn.fwd(q.cuda(), k.cuda(), v.cuda(), return_lse=False)
+    assert none is None and torch.equal(o_dev, o_nolse)
+    o_host, lse_host = attn.fwd(q, k, v)              # host tensors: copies inside the call
+    assert not o_host.is_cuda and torch.equal(o_host, o_dev.cpu()) and torch.equal(lse_host, lse_dev.cpu())
+
+
+def test_empty_and_rejected_calls_leave_outputs_untouched():
+    q = torch.zeros(0, 2, 256, 128, dtype=torch.bfloat16, device="cuda")
+    o, lse = attn.fwd(q, q, q)
+    assert o.shape == (0, 2, 256, 128)
+    qq = torch.randn(1, 1, 128, 128, device="cuda").bfloat16()
+    k0 = torch.zeros(1, 1, 0, 128, dtype=torch.bfloat16, device="cuda")
+    o = torch.full_like(qq, 7.0)
+    with pytest.raises(attn.AttnError) as e:
+        attn.fwd_into(qq, k0, k0, o)
+    assert e.value.status == attn.ATTN_ERR_INVALID_ARG
+    assert bool((o == 7.0).all())
+
+
+# ------------------------------------------------------------- full-size workloads
+
+def _rows_sample(w, n_random, seed):
+    p = attn.plan(w.B, w.H, w.Sq, w.Sk, w.D)
+    bh, rows = [], []
+    # first and last row of each Q tile of a few heads, and every CTA's last work item
+    for h in (0, w.B * w.H - 1):
+        for t in range(0, w.Sq // 128, max(1, w.Sq // 128 // 8)):
+            bh += [h, h]
+            rows += [t * 128, t * 128 + 127]
+    for cta in range(0, p["grid"], 7):
+        last = cta + ((p["work_items"] - 1 - cta) // p["grid"]) * p["grid"]
+        b, qt0, nq = attn.work_item(last, w.B, w.H, w.Sq)
+        bh += [b] * 2
+        rows += [qt0 * 128 + 5, (qt0 + nq - 1) * 128 + 126]
+    rng = np.random.Generator(np.random.PCG64(seed))
+    bh += list(rng.integers(0, w.B * w.H, n_random))
+    rows += list(rng.integers(0, w.Sq, n_random))
+    return np.array(bh), np.array(rows)
+
+
+@pytest.mark.parametrize("name", ["S=4K", "S=8K", "S=16K", "S=12K,H=24"])
+def test_full_size_workload_sampled_rows(name):
+    w = wl.ALL[name]
+    qb, kb, vb = wl.workload_inputs_bits(w)
+    o, lse = _run(qb, kb, vb, w.scale)
+    bh, rows = _rows_sample(w, 400, seed=1)
+    o_ref, lse_ref = oracle.attn_fwd_rows(qb, kb, vb, w.scale, bh, rows)
+    D = w.D
+    _assert_close(o.reshape(-1, w.Sq, D)[bh, rows], o_ref, lse.reshape(-1, w.Sq)[bh, rows], lse_ref)
+    # properties at every row: outputs are convex combinations of V rows
+    v = wl.bf16_bits_to_f32(vb).reshape(-1, w.Sk, D)
+    vmin, vmax = v.min(axis=1), v.max(axis=1)
+    o3 = o.reshape(-1, w.Sq, D)
+    assert (o3 >= vmin[:, None, :] - 1e-2).all() and (o3 <= vmax[:, None, :] + 1e-2).all()
+    assert np.isfinite(lse).all()

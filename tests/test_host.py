@@ -1,0 +1,147 @@
+"""Host-side checks of the CUDA library (no GPU needed).
+
+The shared library must build for sm_103a, load, and export every function
+include/attn_fwd.h declares; its host-only helpers (plan, work-item decoding,
+argument checks that fail before any CUDA call) are checked here against the
+work-decomposition numbers printed in "B200 Attention Kernel from Scratch to
+Near-SOTA in 60 Diagrams", Chapter 14 (tests/golden/work_decomposition.txt).
+"""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from dense_attention_forward_attn_gb300 import attn, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn_fwd.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden", "work_decomposition.txt")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return attn.library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*(attn_[a-z_]+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    assert "attn_fwd" in names and "attn_status_string" in names
+    assert set(names) == set(attn.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(attn.lib_path())
+    for name in _declared_functions():
+        assert hasattr(raw, name), name
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4):
+        assert attn.status_string(code)
+    assert attn.status_string(12345) == "unknown status"
+
+
+def _golden_rows():
+    rows = []
+    for line in open(GOLDEN):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            rows.append([c.strip() for c in line.split("|")])
+    return rows
+
+
+def test_plan_matches_worked_work_decomposition(lib):
+    for name, B, H, S, value, _what in _golden_rows():
+        B, H, S = int(B), int(H), int(S)
+        p = attn.plan(B, H, S, S, 128, num_sms=148)
+        if name.startswith("items_per_head"):
+            assert p["work_items"] // (B * H) == int(value), name
+        elif name.startswith("items_total"):
+            assert p["work_items"] == int(value), name
+        elif name.startswith("waves"):
+            assert math.ceil(p["work_items"] / p["grid"]) == int(value), name
+        elif name.startswith("kv_iters"):
+            assert p["kv_tiles"] == int(value), name
+        elif name.startswith("cta0_tiles"):
+            tiles = []
+            for item in range(0, 3 * p["grid"], p["grid"]):   # work_id += gridDim.x
+                bh, qt0, nq = attn.work_item(item, B, H, S)
+                tiles += [bh * p["q_tiles"] + qt0 + i for i in range(nq)]
+            assert tiles == [int(t) for t in value.split(",")], name
+        else:
+            raise AssertionError(f"unknown golden row {name}")
+
+
+def test_plan_resources_fit_one_sm(lib):
+    p = attn.plan(4, 16, 4096, 4096, 128, num_sms=152)
+    assert p["grid"] == 152 and p["work_items"] == 1024 and p["threads"] == 512
+    assert p["smem_bytes"] <= 227 * 1024      # opt-in shared memory per block
+    assert p["tmem_cols"] == 512              # S0 | S1 | O0 | O1, 128 columns each
+    small = attn.plan(1, 2, 256, 256, 128, num_sms=152)
+    assert small["grid"] == 2 and small["work_items"] == 2
+
+
+def test_work_items_cover_every_q_tile_once(lib):
+    for B, H, S in ((1, 3, 384), (2, 2, 1024), (1, 1, 128)):
+        p = attn.plan(B, H, S, 128, 128, num_sms=152)
+        seen = set()
+        for item in range(p["work_items"]):
+            bh, qt0, nq = attn.work_item(item, B, H, S)
+            for t in range(qt0, qt0 + nq):
+                assert (bh, t) not in seen
+                seen.add((bh, t))
+        assert seen == {(bh, t) for bh in range(B * H) for t in range(S // 128)}
+        with pytest.raises(attn.AttnError):
+            attn.work_item(p["work_items"], B, H, S)
+
+
+def _call(lib, q=16, k=32, v=48, o=64, lse=None, B=1, H=1, Sq=128, Sk=128, D=128, scale=0.1):
+    vp = ctypes.c_void_p
+    return lib.attn_fwd(vp(q) if q else None, vp(k) if k else None, vp(v) if v else None,
+                        vp(o) if o else None, vp(lse) if lse else None, B, H, Sq, Sk, D, scale, None)
+
+
+def test_argument_checks_before_any_cuda_call(lib):
+    big = 1 << 40   # fake, never dereferenced: every case below fails on the host first
+    base = dict(q=big, k=2 * big, v=3 * big, o=4 * big)
+    assert _call(lib, **base, D=64) == attn.ATTN_ERR_UNSUPPORTED
+    assert _call(lib, **base, D=0) == attn.ATTN_ERR_INVALID_ARG
+    assert _call(lib, **base, Sq=100) == attn.ATTN_ERR_UNSUPPORTED
+    assert _call(lib, **base, Sk=130) == attn.ATTN_ERR_UNSUPPORTED
+    assert _call(lib, **base, B=-1) == attn.ATTN_ERR_INVALID_ARG
+    assert _call(lib, **base, Sk=0) == attn.ATTN_ERR_INVALID_ARG
+    assert _call(lib, **base, scale=float("nan")) == attn.ATTN_ERR_INVALID_ARG
+    assert _call(lib, **base, scale=float("inf")) == attn.ATTN_ERR_INVALID_ARG
+    assert _call(lib, **base, scale=-0.5) == attn.ATTN_ERR_UNSUPPORTED
+    assert _call(lib, **dict(base, q=0)) == attn.ATTN_ERR_INVALID_ARG
+    assert _call(lib, **dict(base, o=big + 8)) == attn.ATTN_ERR_INVALID_ARG        # misaligned
+    assert _call(lib, **dict(base, o=big + 4096)) == attn.ATTN_ERR_INVALID_ARG     # o overlaps q
+    assert _call(lib, **base, lse=5 * big + 2) == attn.ATTN_ERR_INVALID_ARG        # misaligned lse
+    assert _call(lib, **base, lse=4 * big + 64) == attn.ATTN_ERR_INVALID_ARG       # lse inside o
+
+
+def test_empty_problems_are_ok_without_launch(lib):
+    assert _call(lib, q=0, k=0, v=0, o=0, B=0) == attn.ATTN_OK
+    assert _call(lib, q=0, k=0, v=0, o=0, H=0) == attn.ATTN_OK
+    assert _call(lib, q=0, k=0, v=0, o=0, Sq=0) == attn.ATTN_OK
+    assert attn.plan(0, 4, 256, 256, 128, num_sms=152)["work_items"] == 0
+
+
+def test_binding_rejects_bad_tensors():
+    import torch
+    q = torch.zeros(1, 1, 128, 128, dtype=torch.float32)
+    with pytest.raises(TypeError):
+        attn.fwd(q, q, q)
+    qb = torch.zeros(1, 1, 128, 256, dtype=torch.bfloat16)[..., :128]
+    with pytest.raises(ValueError):
+        attn.fwd(qb, qb, qb)
