@@ -42,6 +42,11 @@
 #ifndef ATTN_KV_STAGES
 #define ATTN_KV_STAGES 3
 #endif
+// 1: one elected lane per warp arrives on the consumer barriers (counts per warp);
+// 0: every thread arrives (counts per thread).
+#ifndef ATTN_ARRIVE_PER_WARP
+#define ATTN_ARRIVE_PER_WARP 1
+#endif
 
 namespace attn {
 
@@ -53,6 +58,7 @@ constexpr int kThreads = 512;
 constexpr uint32_t kTileBytes = kBlockM * kHeadDim * 2;   // 32 KiB
 constexpr uint32_t kSlabBytes = kTileBytes / 2;           // 128 rows x 64 columns (128 B rows)
 constexpr float kRebaseThresholdLog2 = 8.0f;
+constexpr uint32_t kArrivePerWG = ATTN_ARRIVE_PER_WARP ? 4u : 128u;   // arrivals per warpgroup
 
 // Warp roles.
 constexpr int kCorrWarp0 = 8;
@@ -72,6 +78,10 @@ constexpr uint32_t kTmemCols = 512;
 __host__ __device__ constexpr uint32_t col_s(int q) { return q ? 128u : 0u; }
 __host__ __device__ constexpr uint32_t col_o(int q) { return q ? 384u : 256u; }
 constexpr uint32_t kColP = 64;   // packed P sits over S columns 64..127 of its stage
+// The CTA allocates all 512 columns, so its allocation starts at lane 0, column 0.  MMA
+// operands use this constant (checked after the allocation) so the issuing code keeps them in
+// warp-uniform registers.
+constexpr uint32_t kTmemBase = 0;
 
 // Device status bits (bounded waits that expired, by role).
 constexpr unsigned kStatusTimeoutLoad = 1u << 0;
@@ -79,6 +89,7 @@ constexpr unsigned kStatusTimeoutMma = 1u << 1;
 constexpr unsigned kStatusTimeoutSoftmax = 1u << 2;
 constexpr unsigned kStatusTimeoutCorrection = 1u << 3;
 constexpr unsigned kStatusTimeoutDrain = 1u << 4;
+constexpr unsigned kStatusTmemBase = 1u << 5;   // allocation did not start at column 0
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s for own in-flight work
 
@@ -164,6 +175,17 @@ struct Ctx {
   __device__ uint32_t bar(const uint64_t& b) const { return ptx::smem_u32(&b); }
   __device__ uint32_t sq(int q) const { return smem_base + q * kTileBytes; }
   __device__ uint32_t skv(int s) const { return smem_base + (2 + s) * kTileBytes; }
+
+  // Arrival of this warp's share on a barrier counted per warpgroup (kArrivePerWG).
+  // Callers order their own shared-memory / tcgen05 writes before the call.
+  __device__ void arrive(const uint64_t& b) const {
+#if ATTN_ARRIVE_PER_WARP
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bar(b));
+#else
+    ptx::mbar_arrive(bar(b));
+#endif
+  }
 
   // Warp-uniform bounded wait; all 32 lanes call it.  false = timed out or aborted.
   __device__ bool wait(const uint64_t& b, uint32_t parity, unsigned role_bit) const {
@@ -254,33 +276,35 @@ __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const C
 }
 
 // ------------------------------------------------------------------ MMA warp
-__device__ __forceinline__ void issue_qk(const Ctx& c, int q, int kslot) {
+template <int Q>
+__device__ __forceinline__ void issue_qk(const Ctx& c, int kslot) {
   constexpr uint32_t idesc = make_idesc_bf16(128, 128, 0);
-  const uint32_t d = c.tmem + col_s(q);
+  const uint64_t a0 = smem_desc_sw128(c.sq(Q), 16, 1024);
+  const uint64_t b0 = smem_desc_sw128(c.skv(kslot), 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * kSlabBytes + (kk & 3) * 32;
-    const uint64_t a = smem_desc_sw128(c.sq(q) + off, 16, 1024);
-    const uint64_t b = smem_desc_sw128(c.skv(kslot) + off, 16, 1024);
-    ptx::mma_ss(d, a, b, idesc, kk > 0);
+    // K-step kk: slab kk/4 (64 columns), 32-byte column offset inside the 128-byte swizzle row.
+    const uint32_t off16 = ((kk >> 2) * kSlabBytes + (kk & 3) * 32) >> 4;
+    ptx::mma_ss(kTmemBase + col_s(Q), a0 + off16, b0 + off16, idesc, kk > 0);
   }
 }
 
-// K-steps [k0, k1) of P_q * V: A = packed P in TMEM, B = V tile (MN-major, 128B swizzle).
-__device__ __forceinline__ void issue_pv(const Ctx& c, int q, int vslot, int k0, int k1,
-                                         bool overwrite_first) {
+// K-steps [K0, K1) of P_q * V: A = packed P in TMEM, B = V tile (MN-major, 128B swizzle).
+template <int Q, int K0, int K1>
+__device__ __forceinline__ void issue_pv(const Ctx& c, int vslot, bool overwrite_first) {
   constexpr uint32_t idesc = make_idesc_bf16(128, 128, 1);
-  const uint32_t d = c.tmem + col_o(q);
-  const uint32_t a0 = c.tmem + col_s(q) + kColP;
-  for (int kk = k0; kk < k1; ++kk) {
-    const uint64_t b = smem_desc_sw128(c.skv(vslot) + kk * 16 * 128, kSlabBytes, 1024);
-    ptx::mma_ts(d, a0 + kk * 8, b, idesc, !(overwrite_first && kk == k0));
+  const uint64_t b0 = smem_desc_sw128(c.skv(vslot), kSlabBytes, 1024);
+#pragma unroll
+  for (int kk = K0; kk < K1; ++kk) {
+    // 16 V rows per K-step: 16 * 128 bytes inside each 64-column slab.
+    ptx::mma_ts(kTmemBase + col_o(Q), kTmemBase + col_s(Q) + kColP + kk * 8,
+                b0 + ((kk * 16 * 128) >> 4), idesc, (kk == K0 && overwrite_first) ? 0u : 1u);
   }
 }
 
 __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
   SmemCtl* ctl = c.ctl;
-  const bool leader = c.lane == 0;
+  const bool leader = ptx::elect_one();
   int slot = 0;
   uint32_t phase = 0;
   uint32_t q_cnt[2] = {0, 0};
@@ -301,7 +325,7 @@ __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
     }
     ptx::tc_fence_after();
     if (leader) {
-      issue_qk(c, q, kslot);
+      if (q == 0) issue_qk<0>(c, kslot); else issue_qk<1>(c, kslot);
       ptx::mma_commit(c.bar(ctl->s_full[q]));
       if (last_qk) ptx::mma_commit(c.bar(ctl->q_empty[q]));
       if (release_k) ptx::mma_commit(c.bar(ctl->kv_empty[kslot]));
@@ -312,11 +336,15 @@ __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
   auto pv = [&](int q, int vslot, bool first_tile) -> bool {
     if (!c.wait(ctl->p_hi_full[q], pv_phase[q], kStatusTimeoutMma)) return false;
     ptx::tc_fence_after();
-    if (leader) issue_pv(c, q, vslot, 2, 8, first_tile);
+    if (leader) {
+      if (q == 0) issue_pv<0, 2, 8>(c, vslot, first_tile); else issue_pv<1, 2, 8>(c, vslot, first_tile);
+    }
     __syncwarp();
     if (!c.wait(ctl->p_lo_full[q], pv_phase[q], kStatusTimeoutMma)) return false;
     ptx::tc_fence_after();
-    if (leader) issue_pv(c, q, vslot, 0, 2, false);
+    if (leader) {
+      if (q == 0) issue_pv<0, 0, 2>(c, vslot, false); else issue_pv<1, 0, 2>(c, vslot, false);
+    }
     __syncwarp();
     pv_phase[q] ^= 1u;
     return true;
@@ -418,7 +446,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
         m_kept = m_tile;
       }
       ctl->alpha[q][tphase][row] = alpha;
-      ptx::mbar_arrive(c.bar(ctl->stats_full[q]));
+      c.arrive(ctl->stats_full[q]);
 
       const float neg_m = -m_kept;
       float sum[4];
@@ -440,18 +468,18 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
         if (cc == 1) {
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
-          ptx::mbar_arrive(c.bar(ctl->p_hi_full[q]));
+          c.arrive(ctl->p_hi_full[q]);
         }
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(c.bar(ctl->p_lo_full[q]));
+      c.arrive(ctl->p_lo_full[q]);
       l += (sum[3] + sum[2]) + (sum[1] + sum[0]);
       tphase ^= 1u;
     }
     ctl->row_m[q][items_q & 1u][row] = m_kept;
     ctl->row_l[q][items_q & 1u][row] = l;
-    ptx::mbar_arrive(c.bar(ctl->final_full[q]));
+    c.arrive(ctl->final_full[q]);
     ++items_q;
   }
 }
@@ -527,7 +555,7 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
           ptx::tmem_wait_st();
         }
         ptx::tc_fence_before();
-        ptx::mbar_arrive(c.bar(ctl->p_hi_full[q]));
+        c.arrive(ctl->p_hi_full[q]);
         tphase[q] ^= 1u;
       }
     }
@@ -562,11 +590,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ptx::mbar_init(c.bar(ctl->q_full[q]), 1);
       ptx::mbar_init(c.bar(ctl->q_empty[q]), 1);
       ptx::mbar_init(c.bar(ctl->s_full[q]), 1);
-      ptx::mbar_init(c.bar(ctl->p_hi_full[q]), 2 * 128);   // softmax rows + correction rows
-      ptx::mbar_init(c.bar(ctl->p_lo_full[q]), 128);
-      ptx::mbar_init(c.bar(ctl->stats_full[q]), 128);
+      ptx::mbar_init(c.bar(ctl->p_hi_full[q]), 2 * kArrivePerWG);   // softmax + correction WGs
+      ptx::mbar_init(c.bar(ctl->p_lo_full[q]), kArrivePerWG);
+      ptx::mbar_init(c.bar(ctl->stats_full[q]), kArrivePerWG);
       ptx::mbar_init(c.bar(ctl->o_full[q]), 1);
-      ptx::mbar_init(c.bar(ctl->final_full[q]), 128);
+      ptx::mbar_init(c.bar(ctl->final_full[q]), kArrivePerWG);
     }
     for (int s = 0; s < kKvStages; ++s) {
       ptx::mbar_init(c.bar(ctl->kv_full[s]), 1);
@@ -588,9 +616,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  c.tmem = ctl->tmem_base;
-
-  if (c.warp < kCorrWarp0) {
+  const uint32_t tmem_alloc_base = ctl->tmem_base;
+  c.tmem = kTmemBase;
+  if (tmem_alloc_base != kTmemBase) {
+    if (threadIdx.x == 0) atomicOr(&g_attn_status, kStatusTmemBase);
+  } else if (c.warp < kCorrWarp0) {
     ptx::setmaxnreg_inc<kRegSoftmax>();
     softmax_role(c, p, static_cast<int>(c.warp >> 2));
   } else if (c.warp < kLoadWarp) {
@@ -606,7 +636,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   __syncthreads();
   if (c.warp == kMmaWarp) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(c.tmem, kTmemCols);
+    ptx::tmem_dealloc(tmem_alloc_base, kTmemCols);
   }
 }
 
