@@ -404,6 +404,23 @@ __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
 }
 
 // ------------------------------------------------------------------ softmax warpgroups
+// Max of the 128 raw scores of this thread's row (bit patterns from tcgen05.ld).
+__device__ __forceinline__ float row_max_128(const uint32_t (&sr)[4][32]) {
+  auto f = [&](int i) { return __uint_as_float(sr[i >> 5][i & 31]); };
+  float a[43];
+#pragma unroll
+  for (int i = 0; i < 42; ++i) a[i] = ptx::fmax3(f(3 * i), f(3 * i + 1), f(3 * i + 2));
+  a[42] = fmaxf(f(126), f(127));
+  float b[15];
+#pragma unroll
+  for (int i = 0; i < 14; ++i) b[i] = ptx::fmax3(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
+  b[14] = a[42];
+  float d[5];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) d[i] = ptx::fmax3(b[3 * i], b[3 * i + 1], b[3 * i + 2]);
+  return fmaxf(ptx::fmax3(d[0], d[1], d[2]), fmaxf(d[3], d[4]));
+}
+
 __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int q) {
   SmemCtl* ctl = c.ctl;
   const uint32_t row_base = 32u * (c.warp & 3u);
@@ -426,17 +443,8 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
       for (int cc = 0; cc < 4; ++cc) ptx::tmem_ld_32x32b_x32(taddr_s + 32 * cc, sr[cc]);
       ptx::tmem_wait_ld();
 
-      // Row max over the raw scores: four independent chains.
-      float mx[4];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        float m = __uint_as_float(sr[cc][0]);
-#pragma unroll
-        for (int i = 1; i < 31; i += 2)
-          m = ptx::fmax3(m, __uint_as_float(sr[cc][i]), __uint_as_float(sr[cc][i + 1]));
-        mx[cc] = fmaxf(m, __uint_as_float(sr[cc][31]));
-      }
-      const float m_tile = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
+      // Row max over the raw scores: a 3-input-max tree (depth 5, 65 instructions).
+      const float m_tile = row_max_128(sr) * scale_log2;
       float alpha = 1.f;
       if (j == 0) {
         m_kept = m_tile;
@@ -448,22 +456,25 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
       ctl->alpha[q][tphase][row] = alpha;
       c.arrive(ctl->stats_full[q]);
 
-      const float neg_m = -m_kept;
-      float sum[4];
+      // P = exp2(s * scale_log2 - m_kept), two columns per packed FMA; row sums in packed adds.
+      const float2 c2 = make_float2(scale_log2, scale_log2);
+      const float2 nm2 = make_float2(-m_kept, -m_kept);
+      float2 sum2[4];
       // Upper 96 columns first (packed P columns 16..63), then publish them.
 #pragma unroll
       for (int cc = 3; cc >= 0; --cc) {
         uint32_t pk[16];
-        float s0 = 0.f, s1 = 0.f;
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ptx::ex2_ftz(fmaf(__uint_as_float(sr[cc][2 * i]), scale_log2, neg_m));
-          const float p1 = ptx::ex2_ftz(fmaf(__uint_as_float(sr[cc][2 * i + 1]), scale_log2, neg_m));
-          s0 += p0;
-          s1 += p1;
-          pk[i] = ptx::pack_bf16x2(p0, p1);
+          float2 x = ptx::ffma2(make_float2(__uint_as_float(sr[cc][2 * i]), __uint_as_float(sr[cc][2 * i + 1])),
+                                c2, nm2);
+          x.x = ptx::ex2_ftz(x.x);
+          x.y = ptx::ex2_ftz(x.y);
+          if (i & 1) acc1 = ptx::fadd2(acc1, x); else acc0 = ptx::fadd2(acc0, x);
+          pk[i] = ptx::pack_bf16x2(x.x, x.y);
         }
-        sum[cc] = s0 + s1;
+        sum2[cc] = ptx::fadd2(acc0, acc1);
         ptx::tmem_st_32x32b_x16(taddr_s + kColP + 16 * cc, pk);
         if (cc == 1) {
           ptx::tmem_wait_st();
@@ -474,7 +485,8 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       c.arrive(ctl->p_lo_full[q]);
-      l += (sum[3] + sum[2]) + (sum[1] + sum[0]);
+      const float2 t2 = ptx::fadd2(ptx::fadd2(sum2[3], sum2[2]), ptx::fadd2(sum2[1], sum2[0]));
+      l += t2.x + t2.y;
       tphase ^= 1u;
     }
     ctl->row_m[q][items_q & 1u][row] = m_kept;
