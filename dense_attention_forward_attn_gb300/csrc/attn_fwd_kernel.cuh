@@ -67,10 +67,16 @@ constexpr int kMmaWarp = 13;
 
 // Register split (setmaxnreg): 2 softmax WGs + correction WG + misc WG.
 // (kRegSoftmax * 2 + kRegCorr + kRegMisc) * 128 threads must equal
-// 65536 = kThreads * 128 (the registers the block is launched with).
-constexpr uint32_t kRegSoftmax = 176;
-constexpr uint32_t kRegCorr = 88;
-constexpr uint32_t kRegMisc = 72;
+// 65536 = kThreads * 128 (the registers the block is launched with).  The softmax warps hold a
+// full 128-column score row; the correction and TMA/MMA roles work in 16-column chunks.
+#ifndef ATTN_REG_SOFTMAX
+#define ATTN_REG_SOFTMAX 216
+#define ATTN_REG_CORR 40
+#define ATTN_REG_MISC 40
+#endif
+constexpr uint32_t kRegSoftmax = ATTN_REG_SOFTMAX;
+constexpr uint32_t kRegCorr = ATTN_REG_CORR;
+constexpr uint32_t kRegMisc = ATTN_REG_MISC;
 static_assert((kRegSoftmax * 2 + kRegCorr + kRegMisc) * 128 == 65536, "register split");
 
 // TMEM columns.
@@ -511,18 +517,17 @@ __device__ __forceinline__ bool epilogue(const Ctx& c, const Params& p, int q, c
   const int grow = (w.qt0 + q) * kBlockM + row;
   uint8_t* out = static_cast<uint8_t*>(p.o) + (static_cast<size_t>(w.bh) * p.sq + grow) * (kHeadDim * 2);
   const uint32_t taddr_o = c.tmem + (row_base << 16) + col_o(q);
-#pragma unroll
-  for (int cc = 0; cc < 4; ++cc) {
-    uint32_t r[32];
-    ptx::tmem_ld_32x32b_x32(taddr_o + 32 * cc, r);
+#pragma unroll 2
+  for (int cc = 0; cc < 8; ++cc) {
+    uint32_t r[16];
+    ptx::tmem_ld_32x32b_x16(taddr_o + 16 * cc, r);
     ptx::tmem_wait_ld();
-    uint32_t pk[16];
+    uint32_t pk[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < 8; ++i)
       pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
-#pragma unroll
-    for (int v = 0; v < 4; ++v)
-      ptx::st_global_v4(out + cc * 64 + v * 16, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+    ptx::st_global_v4(out + cc * 32, pk[0], pk[1], pk[2], pk[3]);
+    ptx::st_global_v4(out + cc * 32 + 16, pk[4], pk[5], pk[6], pk[7]);
   }
   if (p.lse != nullptr)
     p.lse[static_cast<size_t>(w.bh) * p.sq + grow] = (m + log2f(l)) * 0.69314718055994530942f;
@@ -556,13 +561,13 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
           const uint32_t taddr_o = c.tmem + (row_base << 16) + col_o(q);
           ptx::tc_fence_after();
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t r[32];
-            ptx::tmem_ld_32x32b_x32(taddr_o + 32 * cc, r);
+          for (int cc = 0; cc < 8; ++cc) {
+            uint32_t r[16];
+            ptx::tmem_ld_32x32b_x16(taddr_o + 16 * cc, r);
             ptx::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
-            ptx::tmem_st_32x32b_x32(taddr_o + 32 * cc, r);
+            for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a);
+            ptx::tmem_st_32x32b_x16(taddr_o + 16 * cc, r);
           }
           ptx::tmem_wait_st();
         }
