@@ -82,6 +82,8 @@ int encode_bhsd(CUtensorMap* map, const void* base, int64_t bh, int64_t s) {
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return na && nb && x < y + nb && y < x + na;
@@ -94,8 +96,7 @@ int check_shape(int B, int H, int Sq, int Sk, int D) {
   const int64_t bh = static_cast<int64_t>(B) * H;
   if (bh == 0 || Sq == 0) return ATTN_OK;   // empty problem
   if (Sk == 0) return ATTN_ERR_INVALID_ARG;
-  if (Sq % attn::kBlockM != 0 || Sk % attn::kBlockN != 0) return ATTN_ERR_UNSUPPORTED;
-  const int64_t items = bh * ((Sq / attn::kBlockM + 1) / 2);
+  const int64_t items = bh * ((ceil_div(Sq, attn::kBlockM) + 1) / 2);
   if (bh > INT32_MAX || items > INT32_MAX) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
@@ -129,8 +130,8 @@ int attn_fwd_plan(int B, int H, int Sq, int Sk, int D, int num_sms, attn_plan* p
   }
   std::memset(plan, 0, sizeof(*plan));
   const int64_t bh = static_cast<int64_t>(B) * H;
-  plan->q_tiles = Sq / attn::kBlockM;
-  plan->kv_tiles = Sk / attn::kBlockN;
+  plan->q_tiles = ceil_div(Sq, attn::kBlockM);
+  plan->kv_tiles = ceil_div(Sk, attn::kBlockN);
   plan->work_items = (Sq == 0) ? 0 : bh * ((plan->q_tiles + 1) / 2);
   plan->grid = static_cast<int>(plan->work_items < num_sms ? plan->work_items : num_sms);
   plan->threads = attn::kThreads;
@@ -144,7 +145,7 @@ int attn_fwd_work_item(int64_t item, int B, int H, int Sq, int* bh, int* q_tile0
   if (bh == nullptr || q_tile0 == nullptr || n_q_tiles == nullptr) return ATTN_ERR_INVALID_ARG;
   const int rc = check_shape(B, H, Sq, attn::kBlockN, attn::kHeadDim);
   if (rc != ATTN_OK) return rc;
-  const int q_tiles = Sq / attn::kBlockM;
+  const int q_tiles = ceil_div(Sq, attn::kBlockM);
   const int pairs = (q_tiles + 1) / 2;
   const int64_t items = static_cast<int64_t>(B) * H * pairs;
   if (item < 0 || item >= items) return ATTN_ERR_INVALID_ARG;
@@ -192,8 +193,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.o = o;
   p.lse = lse;
   p.sq = Sq;
-  p.q_tiles = Sq / attn::kBlockM;
-  p.kv_tiles = Sk / attn::kBlockN;
+  p.q_tiles = ceil_div(Sq, attn::kBlockM);
+  p.kv_tiles = ceil_div(Sk, attn::kBlockN);
+  p.kv_valid_last = Sk - (p.kv_tiles - 1) * attn::kBlockN;
   p.pairs_per_head = (p.q_tiles + 1) / 2;
   p.num_items = static_cast<int>(bh * p.pairs_per_head);
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);

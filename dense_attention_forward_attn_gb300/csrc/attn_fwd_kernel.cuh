@@ -70,9 +70,9 @@ constexpr int kMmaWarp = 13;
 // 65536 = kThreads * 128 (the registers the block is launched with).  The softmax warps hold a
 // full 128-column score row; the correction and TMA/MMA roles work in 16-column chunks.
 #ifndef ATTN_REG_SOFTMAX
-#define ATTN_REG_SOFTMAX 216
-#define ATTN_REG_CORR 40
-#define ATTN_REG_MISC 40
+#define ATTN_REG_SOFTMAX 208
+#define ATTN_REG_CORR 48
+#define ATTN_REG_MISC 48
 #endif
 constexpr uint32_t kRegSoftmax = ATTN_REG_SOFTMAX;
 constexpr uint32_t kRegCorr = ATTN_REG_CORR;
@@ -123,8 +123,9 @@ struct Params {
   void* o;          // BF16 [BH, Sq, 128]
   float* lse;       // fp32 [BH, Sq] or null
   int sq;
-  int q_tiles;      // Sq / 128
-  int kv_tiles;     // Sk / 128
+  int q_tiles;      // ceil(Sq / 128)
+  int kv_tiles;     // ceil(Sk / 128)
+  int kv_valid_last;  // valid key rows in the last KV tile, 1..128
   int pairs_per_head;
   int num_items;
   float scale_log2; // scale * log2(e)
@@ -410,6 +411,60 @@ __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
 }
 
 // ------------------------------------------------------------------ softmax warpgroups
+// Raw scores of columns >= valid become -inf (they then never hold the row max).
+__device__ __forceinline__ void mask_scores(uint32_t (&sr)[4][32], int valid) {
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (cc * 32 + i >= valid) sr[cc][i] = 0xff800000u;
+}
+
+// P of one KV tile: exp2(s * scale_log2 - m_kept), two columns per packed FMA, packed BF16 into
+// TMEM over the upper half of this stage's S columns; the upper 96 columns are published first
+// (p_hi_full: P*V K-steps 2..7 may start), then the lower 32 (p_lo_full).  With MASK, columns
+// >= valid get P = 0 (also when scale is 0).  Returns the row sum of the tile's fp32 P.
+template <bool MASK>
+__device__ __forceinline__ float produce_p(const Ctx& c, int q, const uint32_t (&sr)[4][32],
+                                           float scale_log2, float m_kept, int valid,
+                                           uint32_t taddr_s) {
+  SmemCtl* ctl = c.ctl;
+  const float2 c2 = make_float2(scale_log2, scale_log2);
+  const float2 nm2 = make_float2(-m_kept, -m_kept);
+  float2 sum2[4];
+#pragma unroll
+  for (int cc = 3; cc >= 0; --cc) {
+    uint32_t pk[16];
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float2 x = ptx::ffma2(make_float2(__uint_as_float(sr[cc][2 * i]), __uint_as_float(sr[cc][2 * i + 1])),
+                            c2, nm2);
+      x.x = ptx::ex2_ftz(x.x);
+      x.y = ptx::ex2_ftz(x.y);
+      if (MASK) {
+        const int col = cc * 32 + 2 * i;
+        x.x = col < valid ? x.x : 0.f;
+        x.y = col + 1 < valid ? x.y : 0.f;
+      }
+      if (i & 1) acc1 = ptx::fadd2(acc1, x); else acc0 = ptx::fadd2(acc0, x);
+      pk[i] = ptx::pack_bf16x2(x.x, x.y);
+    }
+    sum2[cc] = ptx::fadd2(acc0, acc1);
+    ptx::tmem_st_32x32b_x16(taddr_s + kColP + 16 * cc, pk);
+    if (cc == 1) {
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      c.arrive(ctl->p_hi_full[q]);
+    }
+  }
+  ptx::tmem_wait_st();
+  ptx::tc_fence_before();
+  c.arrive(ctl->p_lo_full[q]);
+  const float2 t2 = ptx::fadd2(ptx::fadd2(sum2[3], sum2[2]), ptx::fadd2(sum2[1], sum2[0]));
+  return t2.x + t2.y;
+}
+
 // Max of the 128 raw scores of this thread's row (bit patterns from tcgen05.ld).
 __device__ __forceinline__ float row_max_128(const uint32_t (&sr)[4][32]) {
   auto f = [&](int i) { return __uint_as_float(sr[i >> 5][i & 31]); };
@@ -448,6 +503,10 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) ptx::tmem_ld_32x32b_x32(taddr_s + 32 * cc, sr[cc]);
       ptx::tmem_wait_ld();
+      // The last KV tile of a key sequence that is not a multiple of 128: columns past the end
+      // hold scores of zero-filled key rows; they must not enter the max (and get P = 0 below).
+      const bool partial = j == p.kv_tiles - 1 && p.kv_valid_last < kBlockN;
+      if (partial) mask_scores(sr, p.kv_valid_last);
 
       // Row max over the raw scores: a 3-input-max tree (depth 5, 65 instructions).
       const float m_tile = row_max_128(sr) * scale_log2;
@@ -462,37 +521,8 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
       ctl->alpha[q][tphase][row] = alpha;
       c.arrive(ctl->stats_full[q]);
 
-      // P = exp2(s * scale_log2 - m_kept), two columns per packed FMA; row sums in packed adds.
-      const float2 c2 = make_float2(scale_log2, scale_log2);
-      const float2 nm2 = make_float2(-m_kept, -m_kept);
-      float2 sum2[4];
-      // Upper 96 columns first (packed P columns 16..63), then publish them.
-#pragma unroll
-      for (int cc = 3; cc >= 0; --cc) {
-        uint32_t pk[16];
-        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float2 x = ptx::ffma2(make_float2(__uint_as_float(sr[cc][2 * i]), __uint_as_float(sr[cc][2 * i + 1])),
-                                c2, nm2);
-          x.x = ptx::ex2_ftz(x.x);
-          x.y = ptx::ex2_ftz(x.y);
-          if (i & 1) acc1 = ptx::fadd2(acc1, x); else acc0 = ptx::fadd2(acc0, x);
-          pk[i] = ptx::pack_bf16x2(x.x, x.y);
-        }
-        sum2[cc] = ptx::fadd2(acc0, acc1);
-        ptx::tmem_st_32x32b_x16(taddr_s + kColP + 16 * cc, pk);
-        if (cc == 1) {
-          ptx::tmem_wait_st();
-          ptx::tc_fence_before();
-          c.arrive(ctl->p_hi_full[q]);
-        }
-      }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      c.arrive(ctl->p_lo_full[q]);
-      const float2 t2 = ptx::fadd2(ptx::fadd2(sum2[3], sum2[2]), ptx::fadd2(sum2[1], sum2[0]));
-      l += t2.x + t2.y;
+      l += partial ? produce_p<true>(c, q, sr, scale_log2, m_kept, p.kv_valid_last, taddr_s)
+                   : produce_p<false>(c, q, sr, scale_log2, m_kept, 128, taddr_s);
       tphase ^= 1u;
     }
     ctl->row_m[q][items_q & 1u][row] = m_kept;
@@ -515,6 +545,7 @@ __device__ __forceinline__ bool epilogue(const Ctx& c, const Params& p, int q, c
   const float l = ctl->row_l[q][idx & 1u][row];
   const float inv_l = 1.0f / l;
   const int grow = (w.qt0 + q) * kBlockM + row;
+  const bool store = grow < p.sq;   // rows past a ragged end of Q are computed but not stored
   uint8_t* out = static_cast<uint8_t*>(p.o) + (static_cast<size_t>(w.bh) * p.sq + grow) * (kHeadDim * 2);
   const uint32_t taddr_o = c.tmem + (row_base << 16) + col_o(q);
 #pragma unroll 2
@@ -526,10 +557,12 @@ __device__ __forceinline__ bool epilogue(const Ctx& c, const Params& p, int q, c
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
-    ptx::st_global_v4(out + cc * 32, pk[0], pk[1], pk[2], pk[3]);
-    ptx::st_global_v4(out + cc * 32 + 16, pk[4], pk[5], pk[6], pk[7]);
+    if (store) {
+      ptx::st_global_v4(out + cc * 32, pk[0], pk[1], pk[2], pk[3]);
+      ptx::st_global_v4(out + cc * 32 + 16, pk[4], pk[5], pk[6], pk[7]);
+    }
   }
-  if (p.lse != nullptr)
+  if (p.lse != nullptr && store)
     p.lse[static_cast<size_t>(w.bh) * p.sq + grow] = (m + log2f(l)) * 0.69314718055994530942f;
   ptx::tc_fence_before();
   return true;

@@ -47,7 +47,8 @@ typedef enum attn_status {
  *   v    device, BF16, [B, H, Sk, D] contiguous, read only
  *   o    device, BF16, [B, H, Sq, D] contiguous, written (every element)
  *   lse  device, fp32, [B, H, Sq] contiguous, written; may be NULL (not stored)
- *   B, H, Sq, Sk, D   sizes; supported: D == 128, Sq and Sk multiples of 128
+ *   B, H, Sq, Sk, D   sizes; supported: D == 128, any Sq >= 0 and Sk >= 1 (the last
+ *                     128-row tile of a sequence may be partial)
  *   scale             multiplies Q K^T before the softmax; finite and >= 0
  *                     (the row max is taken on raw scores and then scaled)
  *   stream            a cudaStream_t (NULL = the legacy default stream)
@@ -59,8 +60,8 @@ typedef enum attn_status {
  *
  * Errors: arguments are checked on the host before anything is enqueued; any
  * error returns without launching.  B*H == 0 or Sq == 0 is a valid empty
- * problem: ATTN_OK, nothing launched.  Sk == 0 with Sq > 0 is ATTN_ERR_INVALID_ARG
- * (a softmax over no keys).  Sq or Sk not a multiple of 128, or D != 128, is
+ * problem: ATTN_OK, nothing launched.  Sk == 0 with Sq > 0 is
+ * ATTN_ERR_INVALID_ARG (a softmax over no keys).  D != 128 is
  * ATTN_ERR_UNSUPPORTED.  A device that is not compute capability 10.3 gives
  * ATTN_ERR_ARCH.  A failed launch gives ATTN_ERR_CUDA (the sticky-free launch
  * error is cleared).  Non-finite inputs give unspecified outputs.
@@ -83,11 +84,11 @@ const char* attn_status_string(int status);
  * SM, work_id += gridDim.x).
  */
 typedef struct attn_plan {
-  int64_t work_items;  /* B*H*ceil(Sq/256): (batch*head, pair of Q tiles) */
+  int64_t work_items;  /* B*H*ceil(ceil(Sq/128)/2): (batch*head, pair of Q tiles) */
   int grid;            /* persistent CTAs = min(num_sms, work_items) */
   int threads;         /* threads per CTA */
-  int q_tiles;         /* Sq / 128 per head */
-  int kv_tiles;        /* Sk / 128: KV-loop iterations per work item */
+  int q_tiles;         /* ceil(Sq / 128) per head */
+  int kv_tiles;        /* ceil(Sk / 128): KV-loop iterations per work item */
   int kv_stages;       /* shared-memory K/V ring slots */
   int smem_bytes;      /* dynamic shared memory per CTA */
   int tmem_cols;       /* tensor-memory columns per CTA */
@@ -104,7 +105,9 @@ int attn_fwd_work_item(int64_t item, int B, int H, int Sq, int* bh, int* q_tile0
 /*
  * attn_device_status -- read (and with clear != 0, reset) the current device's
  * status word.  Bit 0..3: a bounded wait inside the kernel expired (TMA,
- * MMA, softmax, correction role); bit 4: a drain of in-flight work expired.
+ * MMA, softmax, correction role); bit 4: a drain of in-flight work expired;
+ * bit 5: the tensor-memory allocation did not start at column 0 (the CTA
+ * skipped its work).
  * Zero means no kernel since the last reset hit a wait limit.  Synchronous:
  * copies 4 bytes from the device (waits for prior work on the legacy stream).
  */

@@ -78,6 +78,33 @@ def test_shapes(shape):
     _full_check(*shape, seed=sum(shape))
 
 
+@pytest.mark.parametrize("shape", [
+    (1, 2, 200, 300),    # both lengths ragged
+    (2, 3, 129, 1),      # a single key: O is that key's value row
+    (1, 1, 1, 1),        # one query, one key
+    (1, 2, 385, 127),    # odd Q-tile count with a 1-row last tile; one partial KV tile
+    (1, 1, 255, 129),    # last KV tile holds one key
+    (2, 2, 64, 700),     # Sq < 128; several KV tiles, last one partial
+])
+def test_ragged_lengths(shape):
+    _full_check(*shape, seed=sum(shape) + 1)
+
+
+def test_ragged_keys_with_zero_scale_and_stress_logits():
+    _full_check(1, 2, 130, 257, seed=5, scale=0.0)
+    _full_check(1, 2, 300, 333, seed=6, qk_std=3.0, spike_every=64, spike_factor=8.0)
+
+
+def test_single_key_copies_its_value_row():
+    qb, kb, vb = wl.make_inputs_bits(2, 2, 77, 1, 128, seed=12)
+    o, lse = _run(qb, kb, vb, 0.3)
+    v = wl.bf16_bits_to_f32(vb).astype(np.float64)
+    assert np.abs(o - np.broadcast_to(v, o.shape)).max() <= 1e-2
+    q = wl.bf16_bits_to_f32(qb).astype(np.float64)
+    s = 0.3 * np.einsum("bhqd,bhkd->bhqk", q, wl.bf16_bits_to_f32(kb).astype(np.float64))[..., 0]
+    assert np.abs(lse - s).max() <= LSE_MAX
+
+
 def test_persistent_loop_over_many_items():
     # 2*100*2 = 400 work items on <= 152 CTAs: every CTA runs 2-3 items and
     # carries barrier phases, the KV ring position and the epilogue across them.

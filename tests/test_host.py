@@ -91,8 +91,15 @@ def test_plan_resources_fit_one_sm(lib):
     assert small["grid"] == 2 and small["work_items"] == 2
 
 
+def test_plan_ragged_lengths_round_tiles_up(lib):
+    p = attn.plan(2, 3, 385, 129, 128, num_sms=152)
+    assert p["q_tiles"] == 4 and p["kv_tiles"] == 2 and p["work_items"] == 2 * 3 * 2
+    p = attn.plan(1, 1, 1, 1, 128, num_sms=152)
+    assert p["q_tiles"] == 1 and p["kv_tiles"] == 1 and p["work_items"] == 1
+
+
 def test_work_items_cover_every_q_tile_once(lib):
-    for B, H, S in ((1, 3, 384), (2, 2, 1024), (1, 1, 128)):
+    for B, H, S in ((1, 3, 384), (2, 2, 1024), (1, 1, 128), (2, 1, 300), (1, 2, 1)):
         p = attn.plan(B, H, S, 128, 128, num_sms=152)
         seen = set()
         for item in range(p["work_items"]):
@@ -100,7 +107,7 @@ def test_work_items_cover_every_q_tile_once(lib):
             for t in range(qt0, qt0 + nq):
                 assert (bh, t) not in seen
                 seen.add((bh, t))
-        assert seen == {(bh, t) for bh in range(B * H) for t in range(S // 128)}
+        assert seen == {(bh, t) for bh in range(B * H) for t in range(-(-S // 128))}
         with pytest.raises(attn.AttnError):
             attn.work_item(p["work_items"], B, H, S)
 
@@ -116,8 +123,6 @@ def test_argument_checks_before_any_cuda_call(lib):
     base = dict(q=big, k=2 * big, v=3 * big, o=4 * big)
     assert _call(lib, **base, D=64) == attn.ATTN_ERR_UNSUPPORTED
     assert _call(lib, **base, D=0) == attn.ATTN_ERR_INVALID_ARG
-    assert _call(lib, **base, Sq=100) == attn.ATTN_ERR_UNSUPPORTED
-    assert _call(lib, **base, Sk=130) == attn.ATTN_ERR_UNSUPPORTED
     assert _call(lib, **base, B=-1) == attn.ATTN_ERR_INVALID_ARG
     assert _call(lib, **base, Sk=0) == attn.ATTN_ERR_INVALID_ARG
     assert _call(lib, **base, scale=float("nan")) == attn.ATTN_ERR_INVALID_ARG
