@@ -62,12 +62,12 @@ def _load():
             lib = ctypes.CDLL(build())
             i64, f64, i32 = ctypes.c_int64, ctypes.c_double, ctypes.c_int
             vp = ctypes.c_void_p
-            lib.oracle_attn_fwd.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, f64, vp, vp, i32]
+            lib.oracle_attn_fwd.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, f64, i32, vp, vp, i32]
             lib.oracle_attn_fwd.restype = i32
-            lib.oracle_attn_fwd_rows.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, f64,
+            lib.oracle_attn_fwd_rows.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, f64, i32,
                                                  vp, vp, i64, vp, vp, i32]
             lib.oracle_attn_fwd_rows.restype = i32
-            lib.oracle_attn_probs.argtypes = [vp, vp, i64, i64, i64, f64, vp]
+            lib.oracle_attn_probs.argtypes = [vp, vp, i64, i64, i64, f64, i32, vp]
             lib.oracle_attn_probs.restype = i32
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = i32
@@ -91,8 +91,10 @@ def max_threads() -> int:
     return int(_load().oracle_max_threads())
 
 
-def attn_fwd(q, k, v, scale: float, nthreads: int = 0):
-    """O [B,H,Sq,D] and LSE [B,H,Sq] in fp64 from BF16 q [B,H,Sq,D], k/v [B,H,Sk,D]."""
+def attn_fwd(q, k, v, scale: float, nthreads: int = 0, causal: bool = False):
+    """O [B,H,Sq,D] and LSE [B,H,Sq] in fp64 from BF16 q [B,H,Sq,D], k/v [B,H,Sk,D].
+
+    causal: query i attends keys j <= i (top-left aligned)."""
     q, k, v = _bits(q), _bits(k), _bits(v)
     B, H, Sq, D = q.shape
     Sk = k.shape[2]
@@ -101,13 +103,15 @@ def attn_fwd(q, k, v, scale: float, nthreads: int = 0):
     o = np.empty((B, H, Sq, D), dtype=np.float64)
     lse = np.empty((B, H, Sq), dtype=np.float64)
     rc = _load().oracle_attn_fwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, B, H, Sq, Sk, D,
-                                 float(scale), o.ctypes.data, lse.ctypes.data, int(nthreads))
+                                 float(scale), int(bool(causal)), o.ctypes.data, lse.ctypes.data,
+                                 int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_attn_fwd failed: {rc}")
     return o, lse
 
 
-def attn_fwd_rows(q, k, v, scale: float, bh_idx, row_idx, nthreads: int = 0):
+def attn_fwd_rows(q, k, v, scale: float, bh_idx, row_idx, nthreads: int = 0,
+                  causal: bool = False):
     """Selected output rows: (O [n,D], LSE [n]) for flattened heads bh_idx and query rows row_idx."""
     q, k, v = _bits(q), _bits(k), _bits(v)
     B, H, Sq, D = q.shape
@@ -120,21 +124,22 @@ def attn_fwd_rows(q, k, v, scale: float, bh_idx, row_idx, nthreads: int = 0):
     o = np.empty((n, D), dtype=np.float64)
     lse = np.empty((n,), dtype=np.float64)
     rc = _load().oracle_attn_fwd_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data, B, H, Sq, Sk,
-                                      D, float(scale), bh_idx.ctypes.data, row_idx.ctypes.data, n,
+                                      D, float(scale), int(bool(causal)), bh_idx.ctypes.data,
+                                      row_idx.ctypes.data, n,
                                       o.ctypes.data, lse.ctypes.data, int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_attn_fwd_rows failed: {rc}")
     return o, lse
 
 
-def attn_probs(q_head, k_head, scale: float):
+def attn_probs(q_head, k_head, scale: float, causal: bool = False):
     """Materialised P = softmax(scale * q k^T) of one head, q [Sq,D], k [Sk,D]."""
     q, k = _bits(q_head), _bits(k_head)
     Sq, D = q.shape
     Sk = k.shape[0]
     p = np.empty((Sq, Sk), dtype=np.float64)
     rc = _load().oracle_attn_probs(q.ctypes.data, k.ctypes.data, Sq, Sk, D, float(scale),
-                                   p.ctypes.data)
+                                   int(bool(causal)), p.ctypes.data)
     if rc != 0:
         raise RuntimeError(f"oracle_attn_probs failed: {rc}")
     return p

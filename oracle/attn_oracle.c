@@ -25,6 +25,13 @@
  * The score row is materialised (Sk doubles), then traversed three times, as
  * in the two-kernel scalar formulation.  No blocking, no online rescaling.
  *
+ * causal != 0 restricts row i to keys j <= i (top-left aligned: query i and
+ * key i share a position, as torch.nn.functional.scaled_dot_product_attention
+ * with is_causal=True does); every row keeps at least key 0.  The pages name
+ * causal masking for the sm90 kernel ("Attention for sm90, Line by Line", the
+ * persistent-flag question) without fixing an alignment; top-left is the plain
+ * reading for Sq == Sk and keeps every row non-empty for any Sq, Sk.
+ *
  * Layout: q [B,H,Sq,D], k and v [B,H,Sk,D], all contiguous BF16 bit patterns
  * (uint16).  o [B,H,Sq,D] fp64, lse [B,H,Sq] fp64.
  */
@@ -50,6 +57,7 @@ static void oracle_row(const uint16_t *q_row, const uint16_t *k_head, const uint
                        int64_t Sk, int64_t D, double scale,
                        double *s, double *o_row, double *lse_out)
 {
+    /* Sk here is the number of keys this row attends (all keys, or i + 1 when causal). */
     for (int64_t j = 0; j < Sk; ++j) {
         const uint16_t *k_row = k_head + j * D;
         double dot = 0.0;
@@ -90,13 +98,20 @@ static int set_threads(int nthreads)
 /* Number of threads the OpenMP runtime will use (1 without OpenMP). */
 int oracle_max_threads(void) { return set_threads(0); }
 
+/* Keys attended by query row i. */
+static int64_t keys_for_row(int64_t i, int64_t Sk, int causal)
+{
+    if (!causal) return Sk;
+    return i + 1 < Sk ? i + 1 : Sk;
+}
+
 /*
  * Full forward.  Returns 0 on success, -1 on a bad argument, -2 when the
  * per-thread score buffer cannot be allocated.
  */
 int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                     int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D,
-                    double scale, double *o, double *lse, int nthreads)
+                    double scale, int causal, double *o, double *lse, int nthreads)
 {
     if (B < 0 || H < 0 || Sq < 0 || Sk <= 0 || D <= 0) return -1;
     set_threads(nthreads);
@@ -113,8 +128,8 @@ int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
         for (int64_t r = 0; r < rows; ++r) {
             if (!s) continue;
             const int64_t bh = r / Sq;
-            oracle_row(q + r * D, k + bh * Sk * D, v + bh * Sk * D, Sk, D, scale,
-                       s, o + r * D, lse + r);
+            oracle_row(q + r * D, k + bh * Sk * D, v + bh * Sk * D,
+                       keys_for_row(r - bh * Sq, Sk, causal), D, scale, s, o + r * D, lse + r);
         }
         free(s);
     }
@@ -128,7 +143,7 @@ int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
  */
 int oracle_attn_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                          int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D,
-                         double scale, const int64_t *bh_idx, const int64_t *row_idx,
+                         double scale, int causal, const int64_t *bh_idx, const int64_t *row_idx,
                          int64_t nrows, double *o_rows, double *lse_rows, int nthreads)
 {
     if (B < 0 || H < 0 || Sq < 0 || Sk <= 0 || D <= 0 || nrows < 0) return -1;
@@ -149,7 +164,8 @@ int oracle_attn_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v
             if (!s) continue;
             const int64_t bh = bh_idx[n];
             oracle_row(q + (bh * Sq + row_idx[n]) * D, k + bh * Sk * D, v + bh * Sk * D,
-                       Sk, D, scale, s, o_rows + n * D, lse_rows + n);
+                       keys_for_row(row_idx[n], Sk, causal), D, scale, s, o_rows + n * D,
+                       lse_rows + n);
         }
         free(s);
     }
@@ -158,27 +174,29 @@ int oracle_attn_fwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v
 
 /*
  * Materialised probabilities P = softmax(scale * Q K^T) for one head,
- * p [Sq, Sk].  For small shapes only (checks that rows sum to one).
+ * p [Sq, Sk] (entries of masked keys are 0).  For small shapes only.
  */
 int oracle_attn_probs(const uint16_t *q_head, const uint16_t *k_head,
-                      int64_t Sq, int64_t Sk, int64_t D, double scale, double *p)
+                      int64_t Sq, int64_t Sk, int64_t D, double scale, int causal, double *p)
 {
     if (Sq < 0 || Sk <= 0 || D <= 0) return -1;
     for (int64_t i = 0; i < Sq; ++i) {
         double *s = p + i * Sk;
-        for (int64_t j = 0; j < Sk; ++j) {
+        const int64_t nk = keys_for_row(i, Sk, causal);
+        for (int64_t j = nk; j < Sk; ++j) s[j] = 0.0;
+        for (int64_t j = 0; j < nk; ++j) {
             double dot = 0.0;
             for (int64_t d = 0; d < D; ++d)
                 dot += bf16_to_f64(q_head[i * D + d]) * bf16_to_f64(k_head[j * D + d]);
             s[j] = scale * dot;
         }
         double m = -INFINITY;
-        for (int64_t j = 0; j < Sk; ++j)
+        for (int64_t j = 0; j < nk; ++j)
             if (s[j] > m) m = s[j];
         double l = 0.0;
-        for (int64_t j = 0; j < Sk; ++j)
+        for (int64_t j = 0; j < nk; ++j)
             l += exp(s[j] - m);
-        for (int64_t j = 0; j < Sk; ++j)
+        for (int64_t j = 0; j < nk; ++j)
             s[j] = exp(s[j] - m) / l;
     }
     return 0;

@@ -260,3 +260,62 @@ def test_online_gap_20_without_rebase_grows_p():
     o, lse, reb, m_kept, rowsum = _two_tile_row(20.0, threshold=1e300)
     assert reb[0] == 1 and rowsum[0] - 1.0 == printed   # largest P = 1,048,576
     np.testing.assert_allclose(lse, np.log(1.0 + 2.0 ** 20), rtol=1e-14)
+
+
+# ---------------------------------------------------------------- causal (top-left aligned)
+
+def _sdpa_causal(qb, kb, vb, scale):
+    q, k, v = _f64(qb), _f64(kb), _f64(vb)
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, scale=scale, is_causal=True)
+    Sq, Sk = q.shape[2], k.shape[2]
+    mask = torch.ones(Sq, Sk, dtype=torch.bool).tril(diagonal=0)
+    s = (scale * (q @ k.transpose(-1, -2))).masked_fill(~mask, float("-inf"))
+    return o.numpy(), torch.logsumexp(s, dim=-1).numpy()
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 64, 64, 128), (2, 1, 40, 90, 16), (1, 2, 90, 40, 16),
+                                   (1, 1, 130, 130, 32)])
+def test_causal_oracle_matches_library_sdpa_f64(shape):
+    B, H, Sq, Sk, D = shape
+    qb, kb, vb = wl.make_inputs_bits(B, H, Sq, Sk, D, seed=31)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = oracle.attn_fwd(qb, kb, vb, scale, causal=True)
+    o_ref, lse_ref = _sdpa_causal(qb, kb, vb, scale)
+    np.testing.assert_allclose(o, o_ref, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_causal_oracle_matches_fsum_bruteforce():
+    B, H, Sq, Sk, D = 1, 1, 6, 4, 8
+    qb, kb, vb = wl.make_inputs_bits(B, H, Sq, Sk, D, seed=32, qk_std=2.0)
+    q, k, v = (online.bf16_bits_to_f64(x)[0, 0] for x in (qb, kb, vb))
+    o, lse = oracle.attn_fwd(qb, kb, vb, 0.5, causal=True)
+    for i in range(Sq):
+        keys = range(min(i + 1, Sk))
+        s = [0.5 * math.fsum(q[i, d] * k[j, d] for d in range(D)) for j in keys]
+        m = max(s)
+        e = [math.exp(x - m) for x in s]
+        l = math.fsum(e)
+        for d in range(D):
+            ref = math.fsum(e[n] * v[j, d] for n, j in enumerate(keys)) / l
+            assert abs(o[0, 0, i, d] - ref) <= 1e-14 * max(1.0, abs(ref))
+        assert abs(lse[0, 0, i] - (m + math.log(l))) <= 1e-14 * max(1.0, abs(m))
+
+
+def test_causal_closed_forms():
+    qb, kb, vb = wl.make_inputs_bits(1, 2, 50, 30, 16, seed=33)
+    o_c, l_c = oracle.attn_fwd(qb, kb, vb, 0.4, causal=True)
+    o_n, l_n = oracle.attn_fwd(qb, kb, vb, 0.4)
+    v = online.bf16_bits_to_f64(vb)
+    q, k = online.bf16_bits_to_f64(qb), online.bf16_bits_to_f64(kb)
+    # row 0 sees only key 0
+    np.testing.assert_allclose(o_c[:, :, 0], v[:, :, 0], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(l_c[:, :, 0], 0.4 * (q[:, :, 0] * k[:, :, 0]).sum(-1), rtol=1e-14)
+    # rows at or past the last key see every key
+    np.testing.assert_array_equal(o_c[:, :, 29:], o_n[:, :, 29:])
+    np.testing.assert_array_equal(l_c[:, :, 29:], l_n[:, :, 29:])
+    p = oracle.attn_probs(qb[0, 0], kb[0, 0], 0.4, causal=True)
+    assert (np.triu(p[:30, :30], 1) == 0).all()
+    np.testing.assert_allclose(p.sum(axis=1), 1.0, atol=1e-14)
+    o_r, l_r = oracle.attn_fwd_rows(qb, kb, vb, 0.4, [0, 1, 1], [0, 7, 49], causal=True)
+    np.testing.assert_array_equal(o_r, o_c.reshape(2, 50, 16)[[0, 1, 1], [0, 7, 49]])
