@@ -22,6 +22,7 @@ ATTN_ERR_INVALID_ARG = -1
 ATTN_ERR_UNSUPPORTED = -2
 ATTN_ERR_ARCH = -3
 ATTN_ERR_CUDA = -4
+ATTN_FLAG_CAUSAL = 1
 
 
 class AttnError(RuntimeError):
@@ -36,8 +37,8 @@ class _Plan(ctypes.Structure):
                 ("smem_bytes", ctypes.c_int), ("tmem_cols", ctypes.c_int)]
 
 
-EXPORTS = ("attn_fwd", "attn_status_string", "attn_fwd_plan", "attn_fwd_work_item",
-           "attn_device_status")
+EXPORTS = ("attn_fwd", "attn_fwd_ex", "attn_status_string", "attn_fwd_plan", "attn_fwd_work_item",
+           "attn_fwd_schedule", "attn_device_status")
 
 
 def lib_path() -> str:
@@ -48,13 +49,17 @@ def _bind(lib):
     vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
     lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, vp]
     lib.attn_fwd.restype = i32
+    lib.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp]
+    lib.attn_fwd_ex.restype = i32
     lib.attn_status_string.argtypes = [i32]
     lib.attn_status_string.restype = ctypes.c_char_p
-    lib.attn_fwd_plan.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(_Plan)]
+    lib.attn_fwd_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(_Plan)]
     lib.attn_fwd_plan.restype = i32
-    lib.attn_fwd_work_item.argtypes = [i64, i32, i32, i32, ctypes.POINTER(i32),
-                                       ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    ip = ctypes.POINTER(i32)
+    lib.attn_fwd_work_item.argtypes = [i64, i32, i32, i32, i32, i32, ip, ip, ip, ip]
     lib.attn_fwd_work_item.restype = i32
+    lib.attn_fwd_schedule.argtypes = [i32, i32, i32, i64, i32]
+    lib.attn_fwd_schedule.restype = i32
     lib.attn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
     lib.attn_device_status.restype = i32
     return lib
@@ -80,21 +85,33 @@ def status_string(status: int) -> str:
     return library().attn_status_string(int(status)).decode()
 
 
-def plan(B: int, H: int, Sq: int, Sk: int, D: int = 128, num_sms: int = 0) -> dict:
+def _flags(causal: bool) -> int:
+    return ATTN_FLAG_CAUSAL if causal else 0
+
+
+def plan(B: int, H: int, Sq: int, Sk: int, D: int = 128, num_sms: int = 0,
+         causal: bool = False) -> dict:
     p = _Plan()
-    rc = library().attn_fwd_plan(B, H, Sq, Sk, D, num_sms, ctypes.byref(p))
+    rc = library().attn_fwd_plan(B, H, Sq, Sk, D, _flags(causal), num_sms, ctypes.byref(p))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_plan")
     return {f: getattr(p, f) for f, _ in _Plan._fields_}
 
 
-def work_item(item: int, B: int, H: int, Sq: int):
-    bh, qt0, nq = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-    rc = library().attn_fwd_work_item(item, B, H, Sq, ctypes.byref(bh), ctypes.byref(qt0),
-                                      ctypes.byref(nq))
+def work_item(item: int, B: int, H: int, Sq: int, Sk: int | None = None, causal: bool = False):
+    """(bh, first Q tile, KV tiles of Q tile 0, KV tiles of Q tile 1 or 0)."""
+    bh, qt0, n0, n1 = (ctypes.c_int() for _ in range(4))
+    rc = library().attn_fwd_work_item(item, B, H, Sq, Sq if Sk is None else Sk, _flags(causal),
+                                      ctypes.byref(bh), ctypes.byref(qt0), ctypes.byref(n0),
+                                      ctypes.byref(n1))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_work_item")
-    return bh.value, qt0.value, nq.value
+    return bh.value, qt0.value, n0.value, n1.value
+
+
+def schedule(cta: int, rnd: int, grid: int, work_items: int, causal: bool = False) -> int:
+    """Work item CTA `cta` runs in its rnd-th turn, -1 when it has none left."""
+    return int(library().attn_fwd_schedule(cta, rnd, grid, work_items, _flags(causal)))
 
 
 def device_status(clear: bool = False) -> int:
@@ -113,7 +130,8 @@ def _check(t, name):
         raise ValueError(f"{name} must be contiguous ([B, H, S, D] row-major)")
 
 
-def fwd_into(q, k, v, o, lse=None, scale: float | None = None, stream=None) -> None:
+def fwd_into(q, k, v, o, lse=None, scale: float | None = None, stream=None,
+             causal: bool = False) -> None:
     """Device tensors only: write softmax(scale q k^T) v into `o` (and LSE into `lse`)."""
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
@@ -129,14 +147,14 @@ def fwd_into(q, k, v, o, lse=None, scale: float | None = None, stream=None) -> N
         scale = 1.0 / math.sqrt(D)
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
-    rc = library().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                            lse.data_ptr() if lse is not None else None, B, H, Sq, Sk, D,
-                            float(scale), stream)
+    rc = library().attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               lse.data_ptr() if lse is not None else None, B, H, Sq, Sk, D,
+                               float(scale), _flags(causal), stream)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
 
 
-def fwd(q, k, v, scale: float | None = None, return_lse: bool = True):
+def fwd(q, k, v, scale: float | None = None, return_lse: bool = True, causal: bool = False):
     """Attention forward.  q [B,H,Sq,D], k/v [B,H,Sk,D], BF16 contiguous.
 
     CUDA tensors: runs on the current stream, returns (o, lse) on the device.
@@ -153,7 +171,7 @@ def fwd(q, k, v, scale: float | None = None, return_lse: bool = True):
     B, H, Sq, D = q.shape
     o = torch.empty((B, H, Sq, D), dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device) if return_lse else None
-    fwd_into(q, k, v, o, lse, scale)
+    fwd_into(q, k, v, o, lse, scale, causal=causal)
     if host:
         o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
         o_h.copy_(o, non_blocking=True)

@@ -116,8 +116,9 @@ const char* attn_status_string(int status) {
   }
 }
 
-int attn_fwd_plan(int B, int H, int Sq, int Sk, int D, int num_sms, attn_plan* plan) {
+int attn_fwd_plan(int B, int H, int Sq, int Sk, int D, int flags, int num_sms, attn_plan* plan) {
   if (plan == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (flags & ~ATTN_FLAGS_ALL) return ATTN_ERR_INVALID_ARG;
   const int rc = check_shape(B, H, Sq, Sk, D);
   if (rc != ATTN_OK) return rc;
   if (num_sms <= 0) {
@@ -141,23 +142,42 @@ int attn_fwd_plan(int B, int H, int Sq, int Sk, int D, int num_sms, attn_plan* p
   return ATTN_OK;
 }
 
-int attn_fwd_work_item(int64_t item, int B, int H, int Sq, int* bh, int* q_tile0, int* n_q_tiles) {
-  if (bh == nullptr || q_tile0 == nullptr || n_q_tiles == nullptr) return ATTN_ERR_INVALID_ARG;
-  const int rc = check_shape(B, H, Sq, attn::kBlockN, attn::kHeadDim);
+int attn_fwd_work_item(int64_t item, int B, int H, int Sq, int Sk, int flags, int* bh,
+                       int* q_tile0, int* kv_tiles0, int* kv_tiles1) {
+  if (bh == nullptr || q_tile0 == nullptr || kv_tiles0 == nullptr || kv_tiles1 == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  if (flags & ~ATTN_FLAGS_ALL) return ATTN_ERR_INVALID_ARG;
+  const int rc = check_shape(B, H, Sq, Sk, attn::kHeadDim);
   if (rc != ATTN_OK) return rc;
   const int q_tiles = ceil_div(Sq, attn::kBlockM);
   const int pairs = (q_tiles + 1) / 2;
   const int64_t items = static_cast<int64_t>(B) * H * pairs;
   if (item < 0 || item >= items) return ATTN_ERR_INVALID_ARG;
-  const attn::WorkItem w = attn::decode_item(static_cast<int>(item), pairs, q_tiles);
+  const attn::WorkItem w =
+      attn::decode_item(static_cast<int>(item), pairs, q_tiles, ceil_div(Sk, attn::kBlockN),
+                        B * H, (flags & ATTN_FLAG_CAUSAL) != 0);
   *bh = w.bh;
   *q_tile0 = w.qt0;
-  *n_q_tiles = w.has_q1 ? 2 : 1;
+  *kv_tiles0 = w.n[0];
+  *kv_tiles1 = w.n[1];
   return ATTN_OK;
+}
+
+int attn_fwd_schedule(int cta, int round, int grid, int64_t work_items, int flags) {
+  if (cta < 0 || round < 0 || grid <= 0 || cta >= grid || work_items < 0 || work_items > INT32_MAX)
+    return -1;
+  return attn::item_of(round, cta, grid, static_cast<int>(work_items),
+                       (flags & ATTN_FLAG_CAUSAL) != 0);
 }
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
              int Sq, int Sk, int D, float scale, void* stream) {
+  return attn_fwd_ex(q, k, v, o, lse, B, H, Sq, Sk, D, scale, 0, stream);
+}
+
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int Sq, int Sk, int D, float scale, int flags, void* stream) {
+  if (flags & ~ATTN_FLAGS_ALL) return ATTN_ERR_INVALID_ARG;
   int rc = check_shape(B, H, Sq, Sk, D);
   if (rc != ATTN_OK) return rc;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -198,6 +218,8 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.kv_valid_last = Sk - (p.kv_tiles - 1) * attn::kBlockN;
   p.pairs_per_head = (p.q_tiles + 1) / 2;
   p.num_items = static_cast<int>(bh * p.pairs_per_head);
+  p.bh = static_cast<int>(bh);
+  p.causal = (flags & ATTN_FLAG_CAUSAL) ? 1 : 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   const int grid = p.num_items < info.num_sms ? p.num_items : info.num_sms;
 

@@ -70,8 +70,8 @@ constexpr int kMmaWarp = 13;
 // 65536 = kThreads * 128 (the registers the block is launched with).  The softmax warps hold a
 // full 128-column score row; the correction and TMA/MMA roles work in 16-column chunks.
 #ifndef ATTN_REG_SOFTMAX
-#define ATTN_REG_SOFTMAX 208
-#define ATTN_REG_CORR 48
+#define ATTN_REG_SOFTMAX 200
+#define ATTN_REG_CORR 64
 #define ATTN_REG_MISC 48
 #endif
 constexpr uint32_t kRegSoftmax = ATTN_REG_SOFTMAX;
@@ -128,23 +128,50 @@ struct Params {
   int kv_valid_last;  // valid key rows in the last KV tile, 1..128
   int pairs_per_head;
   int num_items;
+  int bh;           // B * H
+  int causal;       // query i attends keys j <= i (top-left aligned)
   float scale_log2; // scale * log2(e)
 };
 
 struct WorkItem {
   int bh;       // flattened batch*head
   int qt0;      // first Q tile of the pair
-  bool has_q1;  // second Q tile exists (false for the last pair of an odd tile count)
+  int n[2];     // KV tiles attended by Q tile qt0 + q (0: the pair has no second Q tile)
 };
 
-// Work item -> (bh, Q-tile pair); consecutive items walk the Q pairs of one head.
-__host__ __device__ inline WorkItem decode_item(int item, int pairs_per_head, int q_tiles) {
+// Work item -> (bh, Q-tile pair, KV tiles per Q tile).  Dense: consecutive items walk the Q
+// pairs of one head (its K/V stays hot in L2).  Causal: the work of a pair grows with its
+// position, so items are numbered heaviest first (last pair of every head, then the one before).
+__host__ __device__ inline WorkItem decode_item(int item, int pairs_per_head, int q_tiles,
+                                                int kv_tiles, int bh_count, bool causal) {
   WorkItem w;
-  w.bh = item / pairs_per_head;
-  const int pair = item - w.bh * pairs_per_head;
+  int pair;
+  if (causal) {
+    pair = pairs_per_head - 1 - item / bh_count;
+    w.bh = item - (item / bh_count) * bh_count;
+  } else {
+    w.bh = item / pairs_per_head;
+    pair = item - w.bh * pairs_per_head;
+  }
   w.qt0 = 2 * pair;
-  w.has_q1 = (w.qt0 + 1) < q_tiles;
+  const int t1 = w.qt0 + 1;
+  const int c0 = w.qt0 + 1 < kv_tiles ? w.qt0 + 1 : kv_tiles;
+  const int c1 = t1 + 1 < kv_tiles ? t1 + 1 : kv_tiles;
+  w.n[0] = causal ? c0 : kv_tiles;
+  w.n[1] = t1 < q_tiles ? (causal ? c1 : kv_tiles) : 0;
   return w;
+}
+
+__device__ __forceinline__ WorkItem decode_item(int item, const Params& p) {
+  return decode_item(item, p.pairs_per_head, p.q_tiles, p.kv_tiles, p.bh, p.causal != 0);
+}
+
+// The item a persistent CTA runs in its round-th turn, or -1 when it has none left.  Dense:
+// static stride (work_id += gridDim.x).  Causal: every other round runs in reverse CTA order,
+// so the heaviest-first numbering spreads evenly over the CTAs.
+__host__ __device__ inline int item_of(int round, int cta, int grid, int num_items, bool causal) {
+  const int k = round * grid + ((causal && (round & 1)) ? grid - 1 - cta : cta);
+  return k < num_items ? k : -1;
 }
 
 // tcgen05 shared-memory matrix descriptor, 128-byte swizzle.
@@ -264,13 +291,16 @@ __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const C
     return true;
   };
 
-  for (int item = blockIdx.x; ok && item < p.num_items; item += gridDim.x) {
-    const WorkItem w = decode_item(item, p.pairs_per_head, p.q_tiles);
+  for (int r = 0; ok; ++r) {
+    const int item = item_of(r, blockIdx.x, gridDim.x, p.num_items, p.causal != 0);
+    if (item < 0) break;
+    const WorkItem w = decode_item(item, p);
     const int row0 = w.qt0 * kBlockM;
+    const int ntiles = w.n[1] > 0 ? w.n[1] : w.n[0];   // n[1] >= n[0] whenever it is non-zero
     ok = load_q(0, w.bh, row0) && load_kv(tm_k, w.bh, 0);
-    if (ok && w.has_q1) ok = load_q(1, w.bh, row0 + kBlockM);
+    if (ok && w.n[1] > 0) ok = load_q(1, w.bh, row0 + kBlockM);
     if (ok) ok = load_kv(tm_v, w.bh, 0);
-    for (int j = 1; ok && j < p.kv_tiles; ++j)
+    for (int j = 1; ok && j < ntiles; ++j)
       ok = load_kv(tm_k, w.bh, j * kBlockN) && load_kv(tm_v, w.bh, j * kBlockN);
   }
   if (!ok) {
@@ -357,51 +387,72 @@ __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
     return true;
   };
 
-  int item = blockIdx.x;
-  if (item < p.num_items) {
-    WorkItem w = decode_item(item, p.pairs_per_head, p.q_tiles);
-    int j = 0;
+  // K/V tokens are consumed in the order the TMA warp loads them (K_0, V_0, K_1, V_1, ... per
+  // item).  Per KV tile j: P_0 V(j), Q_0 K(j+1), P_1 V(j), Q_1 K(j+1) (Chapter 7 order).  A
+  // stage whose stream ends on the item's last tile issues the next item's first Q K right after
+  // its last P V; a stage that ends earlier (stage 0 of a causal pair) defers it to the end of
+  // the item, after the last token of the item has been consumed.
+  int r = 0;
+  int item = item_of(0, blockIdx.x, gridDim.x, p.num_items, p.causal != 0);
+  if (item >= 0) {
+    WorkItem w = decode_item(item, p);
     int kslot;
-    const bool one_tile = p.kv_tiles == 1;
-    ok = next_kv(kslot) && qk(0, kslot, true, one_tile, !w.has_q1);
-    if (ok && w.has_q1) ok = qk(1, kslot, true, one_tile, true);
+    ok = next_kv(kslot) && qk(0, kslot, true, w.n[0] == 1, w.n[1] == 0);
+    if (ok && w.n[1] > 0) ok = qk(1, kslot, true, w.n[1] == 1, true);
     while (ok) {
-      int vslot;
-      if (!(ok = next_kv(vslot))) break;
-      const bool last_of_item = j == p.kv_tiles - 1;
-      int nitem = item, nj = j + 1;
-      if (last_of_item) { nitem = item + gridDim.x; nj = 0; }
-      const bool has_next = nitem < p.num_items;
-      const WorkItem nw = last_of_item ? (has_next ? decode_item(nitem, p.pairs_per_head, p.q_tiles) : w) : w;
-      const bool next_last_qk = nj == p.kv_tiles - 1;
-
-      // stage 0: P0 V(j), then Q0 K(next)
-      if (!(ok = pv(0, vslot, j == 0))) break;
-      if (leader) {
-        if (last_of_item) ptx::mma_commit(c.bar(ctl->o_full[0]));
-        if (!w.has_q1) ptx::mma_commit(c.bar(ctl->kv_empty[vslot]));
-      }
-      __syncwarp();
-      int nkslot = 0;
-      if (has_next) {
-        if (!(ok = next_kv(nkslot))) break;
-        if (!(ok = qk(0, nkslot, nj == 0, next_last_qk, !nw.has_q1))) break;
-      }
-      // stage 1: P1 V(j), then Q1 K(next)
-      if (w.has_q1) {
-        if (!(ok = pv(1, vslot, j == 0))) break;
-        if (leader) {
-          if (last_of_item) ptx::mma_commit(c.bar(ctl->o_full[1]));
-          ptx::mma_commit(c.bar(ctl->kv_empty[vslot]));
+      const int ntiles = w.n[1] > 0 ? w.n[1] : w.n[0];
+      const int nitem = item_of(r + 1, blockIdx.x, gridDim.x, p.num_items, p.causal != 0);
+      const bool has_next = nitem >= 0;
+      const WorkItem nw = has_next ? decode_item(nitem, p) : w;
+      int next_kslot = -1;
+      // First Q K of stage q for the next item (its K_0 is acquired once for both stages).
+      auto issue_next = [&](int q) -> bool {
+        if (!has_next || nw.n[q] == 0) return true;
+        if (next_kslot < 0 && !next_kv(next_kslot)) return false;
+        return qk(q, next_kslot, true, nw.n[q] == 1, q == 1 || nw.n[1] == 0);
+      };
+      bool next0_done = false;
+      for (int j = 0; ok && j < ntiles; ++j) {
+        int vslot;
+        if (!(ok = next_kv(vslot))) break;
+        int kslot_next = -1;
+        // stage 0: P0 V(j), then Q0 K(j+1)
+        if (j < w.n[0]) {
+          if (!(ok = pv(0, vslot, j == 0))) break;
+          if (leader) {
+            if (j == w.n[0] - 1) ptx::mma_commit(c.bar(ctl->o_full[0]));
+            if (j >= w.n[1]) ptx::mma_commit(c.bar(ctl->kv_empty[vslot]));
+          }
+          __syncwarp();
+          if (j + 1 < w.n[0]) {
+            if (!(ok = next_kv(kslot_next))) break;
+            if (!(ok = qk(0, kslot_next, false, j + 1 == w.n[0] - 1, j + 1 >= w.n[1]))) break;
+          } else if (j == ntiles - 1) {
+            if (!(ok = issue_next(0))) break;
+            next0_done = true;
+          }
         }
-        __syncwarp();
+        // stage 1: P1 V(j), then Q1 K(j+1)
+        if (j < w.n[1]) {
+          if (!(ok = pv(1, vslot, j == 0))) break;
+          if (leader) {
+            if (j == w.n[1] - 1) ptx::mma_commit(c.bar(ctl->o_full[1]));
+            ptx::mma_commit(c.bar(ctl->kv_empty[vslot]));
+          }
+          __syncwarp();
+          if (j + 1 < w.n[1]) {
+            if (kslot_next < 0 && !(ok = next_kv(kslot_next))) break;
+            if (!(ok = qk(1, kslot_next, false, j + 1 == w.n[1] - 1, true))) break;
+          }
+        }
       }
-      if (has_next && nw.has_q1)
-        if (!(ok = qk(1, nkslot, nj == 0, next_last_qk, true))) break;
+      if (!ok) break;
+      if (!next0_done && !(ok = issue_next(0))) break;
+      if (!(ok = issue_next(1))) break;
       if (!has_next) break;
       item = nitem;
-      j = nj;
       w = nw;
+      ++r;
     }
   }
   // Wait for every MMA this thread issued before TMEM can be released.
@@ -491,22 +542,31 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
   uint32_t tphase = 0;
   uint32_t items_q = 0;
 
-  for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
-    const WorkItem w = decode_item(item, p.pairs_per_head, p.q_tiles);
-    if (q == 1 && !w.has_q1) continue;
+  for (int r = 0;; ++r) {
+    const int item = item_of(r, blockIdx.x, gridDim.x, p.num_items, p.causal != 0);
+    if (item < 0) break;
+    const WorkItem w = decode_item(item, p);
+    const int ntiles = w.n[q];
+    if (ntiles == 0) continue;
+    const int qtile = w.qt0 + q;
     float m_kept = 0.f;   // base-2 units; set on the first tile
     float l = 0.f;
-    for (int j = 0; j < p.kv_tiles; ++j) {
+    for (int j = 0; j < ntiles; ++j) {
       if (!c.wait(ctl->s_full[q], tphase, kStatusTimeoutSoftmax)) return;
       ptx::tc_fence_after();
       uint32_t sr[4][32];
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) ptx::tmem_ld_32x32b_x32(taddr_s + 32 * cc, sr[cc]);
       ptx::tmem_wait_ld();
-      // The last KV tile of a key sequence that is not a multiple of 128: columns past the end
-      // hold scores of zero-filled key rows; they must not enter the max (and get P = 0 below).
-      const bool partial = j == p.kv_tiles - 1 && p.kv_valid_last < kBlockN;
-      if (partial) mask_scores(sr, p.kv_valid_last);
+      // Masked columns (no weight): past the end of a key sequence that is not a multiple of
+      // 128 (zero-filled key rows), and, with the causal mask, past this row on the diagonal
+      // tile.  They must not enter the max and get P = 0 below.  The test is warp-uniform.
+      const bool diag = p.causal != 0 && j == qtile;
+      const bool partial = diag || (j == p.kv_tiles - 1 && p.kv_valid_last < kBlockN);
+      int valid = kBlockN;
+      if (j == p.kv_tiles - 1) valid = p.kv_valid_last;
+      if (diag) valid = min(valid, row + 1);
+      if (partial) mask_scores(sr, valid);
 
       // Row max over the raw scores: a 3-input-max tree (depth 5, 65 instructions).
       const float m_tile = row_max_128(sr) * scale_log2;
@@ -521,8 +581,8 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
       ctl->alpha[q][tphase][row] = alpha;
       c.arrive(ctl->stats_full[q]);
 
-      l += partial ? produce_p<true>(c, q, sr, scale_log2, m_kept, p.kv_valid_last, taddr_s)
-                   : produce_p<false>(c, q, sr, scale_log2, m_kept, 128, taddr_s);
+      l += partial ? produce_p<true>(c, q, sr, scale_log2, m_kept, valid, taddr_s)
+                   : produce_p<false>(c, q, sr, scale_log2, m_kept, kBlockN, taddr_s);
       tphase ^= 1u;
     }
     ctl->row_m[q][items_q & 1u][row] = m_kept;
@@ -577,12 +637,15 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
   bool pending[2] = {false, false};
   WorkItem pend_w[2];
 
-  for (int item = blockIdx.x; item < p.num_items; item += gridDim.x) {
-    const WorkItem w = decode_item(item, p.pairs_per_head, p.q_tiles);
-    for (int j = 0; j < p.kv_tiles; ++j) {
+  for (int r = 0;; ++r) {
+    const int item = item_of(r, blockIdx.x, gridDim.x, p.num_items, p.causal != 0);
+    if (item < 0) break;
+    const WorkItem w = decode_item(item, p);
+    const int ntiles = w.n[1] > 0 ? w.n[1] : w.n[0];
+    for (int j = 0; j < ntiles; ++j) {
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        if (q == 1 && !w.has_q1) continue;
+        if (j >= w.n[q]) continue;
         if (j == 0 && pending[q]) {
           if (!epilogue(c, p, q, pend_w[q], items_done[q])) return;
           ++items_done[q];
@@ -611,7 +674,7 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
     }
     pending[0] = true;
     pend_w[0] = w;
-    if (w.has_q1) {
+    if (w.n[1] > 0) {
       pending[1] = true;
       pend_w[1] = w;
     }

@@ -72,6 +72,24 @@ typedef enum attn_status {
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
              int Sq, int Sk, int D, float scale, void* stream);
 
+/* Flags of attn_fwd_ex. */
+#define ATTN_FLAG_CAUSAL 1 /* query i attends keys j <= i (top-left aligned, i and j from 0) */
+#define ATTN_FLAGS_ALL ATTN_FLAG_CAUSAL
+
+/*
+ * attn_fwd_ex -- attn_fwd with options.  Arguments, ownership, errors and
+ * asynchrony as attn_fwd; flags is a bitwise OR of ATTN_FLAG_* (0 = attn_fwd),
+ * other bits give ATTN_ERR_INVALID_ARG.
+ *
+ * ATTN_FLAG_CAUSAL: the causal mask, key j is used by query i only when
+ * j <= i, i.e. the two sequences are aligned at their first positions; every
+ * query keeps at least key 0.  "Attention for sm90, Line by Line" (the
+ * persistent-flag question) names causal masking and the load imbalance it
+ * brings to a persistent schedule; work items are then run heaviest first.
+ */
+int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int Sq, int Sk, int D, float scale, int flags, void* stream);
+
 /* Static text for a status code (never NULL). */
 const char* attn_status_string(int status);
 
@@ -94,13 +112,23 @@ typedef struct attn_plan {
   int tmem_cols;       /* tensor-memory columns per CTA */
 } attn_plan;
 
-int attn_fwd_plan(int B, int H, int Sq, int Sk, int D, int num_sms, attn_plan* plan);
+int attn_fwd_plan(int B, int H, int Sq, int Sk, int D, int flags, int num_sms, attn_plan* plan);
 
 /*
- * attn_fwd_work_item -- which (flattened batch*head, first Q tile, Q-tile
- * count) a work item covers; the same decoding the kernel uses.  Host only.
+ * attn_fwd_work_item -- what work item `item` covers, decoded as the kernel
+ * does: the flattened batch*head, its first Q tile, and the number of KV tiles
+ * each of its two Q tiles attends (kv_tiles1 = 0 when the item has one Q
+ * tile).  Host only.
  */
-int attn_fwd_work_item(int64_t item, int B, int H, int Sq, int* bh, int* q_tile0, int* n_q_tiles);
+int attn_fwd_work_item(int64_t item, int B, int H, int Sq, int Sk, int flags, int* bh,
+                       int* q_tile0, int* kv_tiles0, int* kv_tiles1);
+
+/*
+ * attn_fwd_schedule -- the work item persistent CTA `cta` (of `grid`) runs in
+ * its round-th turn, or -1 when it has none left; the kernel's own schedule.
+ * Host only.
+ */
+int attn_fwd_schedule(int cta, int round, int grid, int64_t work_items, int flags);
 
 /*
  * attn_device_status -- read (and with clear != 0, reset) the current device's

@@ -30,9 +30,9 @@ def _status_clean():
     assert attn.device_status() == 0, "a bounded wait expired inside the kernel"
 
 
-def _run(qb, kb, vb, scale):
+def _run(qb, kb, vb, scale, causal=False):
     q, k, v = (wl.bits_to_torch(x).cuda() for x in (qb, kb, vb))
-    o, lse = attn.fwd(q, k, v, scale=scale)
+    o, lse = attn.fwd(q, k, v, scale=scale, causal=causal)
     torch.cuda.synchronize()
     return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
@@ -46,11 +46,11 @@ def _assert_close(o, o_ref, lse, lse_ref):
     assert lerr.max() <= LSE_MAX, f"LSE max-abs {lerr.max():.4g}"
 
 
-def _full_check(B, H, Sq, Sk, seed=0, scale=None, **kw):
+def _full_check(B, H, Sq, Sk, seed=0, scale=None, causal=False, **kw):
     qb, kb, vb = wl.make_inputs_bits(B, H, Sq, Sk, 128, seed=seed, **kw)
     scale = 1.0 / math.sqrt(128) if scale is None else scale
-    o, lse = _run(qb, kb, vb, scale)
-    o_ref, lse_ref = oracle.attn_fwd(qb, kb, vb, scale)
+    o, lse = _run(qb, kb, vb, scale, causal)
+    o_ref, lse_ref = oracle.attn_fwd(qb, kb, vb, scale, causal=causal)
     _assert_close(o, o_ref, lse, lse_ref)
     return o, lse
 
@@ -184,9 +184,9 @@ def _rows_sample(w, n_random, seed):
             rows += [t * 128, t * 128 + 127]
     for cta in range(0, p["grid"], 7):
         last = cta + ((p["work_items"] - 1 - cta) // p["grid"]) * p["grid"]
-        b, qt0, nq = attn.work_item(last, w.B, w.H, w.Sq)
+        b, qt0, n0, n1 = attn.work_item(last, w.B, w.H, w.Sq, w.Sk)
         bh += [b] * 2
-        rows += [qt0 * 128 + 5, (qt0 + nq - 1) * 128 + 126]
+        rows += [qt0 * 128 + 5, (qt0 + (n1 > 0)) * 128 + 126]
     rng = np.random.Generator(np.random.PCG64(seed))
     bh += list(rng.integers(0, w.B * w.H, n_random))
     rows += list(rng.integers(0, w.Sq, n_random))
@@ -208,3 +208,59 @@ def test_full_size_workload_sampled_rows(name):
     o3 = o.reshape(-1, w.Sq, D)
     assert (o3 >= vmin[:, None, :] - 1e-2).all() and (o3 <= vmax[:, None, :] + 1e-2).all()
     assert np.isfinite(lse).all()
+
+
+# ------------------------------------------------------------- causal (top-left aligned)
+
+@pytest.mark.parametrize("shape", [
+    (1, 2, 256, 256),     # two tiles: pair (0, 1) attends 1 and 2 KV tiles
+    (1, 3, 1024, 1024),   # 4 pairs per head, heaviest first
+    (2, 2, 640, 640),     # odd Q-tile count: the last pair has one Q tile
+    (1, 2, 300, 300),     # ragged: the diagonal tile is also the partial last tile
+    (1, 2, 640, 300),     # Sq > Sk: later Q tiles attend every key
+    (1, 2, 300, 900),     # Sq < Sk: keys past the last query are never used
+    (1, 1, 1, 1),
+])
+def test_causal(shape):
+    _full_check(*shape, seed=sum(shape) + 7, causal=True)
+
+
+def test_causal_stress_logits():
+    w = wl.STRESS
+    _full_check(w.B, w.H, w.Sq, w.Sk, seed=3, qk_std=w.qk_std, spike_every=w.spike_every,
+                spike_factor=w.spike_factor, causal=True)
+
+
+def test_causal_zero_scale_is_prefix_average():
+    qb, kb, vb = wl.make_inputs_bits(1, 1, 384, 384, 128, seed=4)
+    o, lse = _run(qb, kb, vb, 0.0, causal=True)
+    v = wl.bf16_bits_to_f32(vb).astype(np.float64)[0, 0]
+    prefix_mean = np.cumsum(v, axis=0) / np.arange(1, 385)[:, None]
+    assert np.abs(o[0, 0] - prefix_mean).max() <= O_MAX
+    assert np.abs(lse[0, 0] - np.log(np.arange(1, 385))).max() <= LSE_MAX
+
+
+def test_causal_persistent_many_items_and_deterministic():
+    B, H, Sq, Sk = 2, 40, 1024, 1024     # 320 items of unequal work on <= 152 CTAs
+    qb, kb, vb = wl.make_inputs_bits(B, H, Sq, Sk, 128, seed=22)
+    scale = 1.0 / math.sqrt(128)
+    o, lse = _run(qb, kb, vb, scale, causal=True)
+    o2, lse2 = _run(qb, kb, vb, scale, causal=True)
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+    rng = np.random.Generator(np.random.PCG64(6))
+    bh = rng.integers(0, B * H, 2000)
+    rows = rng.integers(0, Sq, 2000)
+    o_ref, lse_ref = oracle.attn_fwd_rows(qb, kb, vb, scale, bh, rows, causal=True)
+    _assert_close(o.reshape(B * H, Sq, 128)[bh, rows], o_ref, lse.reshape(B * H, Sq)[bh, rows], lse_ref)
+
+
+@pytest.mark.parametrize("name", ["S=4K", "S=16K"])
+def test_causal_full_size_sampled_rows(name):
+    w = wl.ALL[name]
+    qb, kb, vb = wl.workload_inputs_bits(w)
+    o, lse = _run(qb, kb, vb, w.scale, causal=True)
+    rng = np.random.Generator(np.random.PCG64(2))
+    bh = np.concatenate([rng.integers(0, w.B * w.H, 300), [0, 0, w.B * w.H - 1]])
+    rows = np.concatenate([rng.integers(0, w.Sq, 300), [0, 127, w.Sq - 1]])
+    o_ref, lse_ref = oracle.attn_fwd_rows(qb, kb, vb, w.scale, bh, rows, causal=True)
+    _assert_close(o.reshape(-1, w.Sq, w.D)[bh, rows], o_ref, lse.reshape(-1, w.Sq)[bh, rows], lse_ref)

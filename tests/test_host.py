@@ -75,8 +75,8 @@ def test_plan_matches_worked_work_decomposition(lib):
         elif name.startswith("cta0_tiles"):
             tiles = []
             for item in range(0, 3 * p["grid"], p["grid"]):   # work_id += gridDim.x
-                bh, qt0, nq = attn.work_item(item, B, H, S)
-                tiles += [bh * p["q_tiles"] + qt0 + i for i in range(nq)]
+                bh, qt0, n0, n1 = attn.work_item(item, B, H, S)
+                tiles += [bh * p["q_tiles"] + qt0 + i for i in range(1 + (n1 > 0))]
             assert tiles == [int(t) for t in value.split(",")], name
         else:
             raise AssertionError(f"unknown golden row {name}")
@@ -101,15 +101,17 @@ def test_plan_ragged_lengths_round_tiles_up(lib):
 def test_work_items_cover_every_q_tile_once(lib):
     for B, H, S in ((1, 3, 384), (2, 2, 1024), (1, 1, 128), (2, 1, 300), (1, 2, 1)):
         p = attn.plan(B, H, S, 128, 128, num_sms=152)
+        assert p["kv_tiles"] == 1
         seen = set()
         for item in range(p["work_items"]):
-            bh, qt0, nq = attn.work_item(item, B, H, S)
-            for t in range(qt0, qt0 + nq):
+            bh, qt0, n0, n1 = attn.work_item(item, B, H, S, 128)
+            assert n0 == 1 and n1 in (0, 1)       # Sk = 128: one KV tile each
+            for t in range(qt0, qt0 + 1 + (n1 > 0)):
                 assert (bh, t) not in seen
                 seen.add((bh, t))
         assert seen == {(bh, t) for bh in range(B * H) for t in range(-(-S // 128))}
         with pytest.raises(attn.AttnError):
-            attn.work_item(p["work_items"], B, H, S)
+            attn.work_item(p["work_items"], B, H, S, 128)
 
 
 def _call(lib, q=16, k=32, v=48, o=64, lse=None, B=1, H=1, Sq=128, Sk=128, D=128, scale=0.1):
@@ -150,3 +152,39 @@ def test_binding_rejects_bad_tensors():
     qb = torch.zeros(1, 1, 128, 256, dtype=torch.bfloat16)[..., :128]
     with pytest.raises(ValueError):
         attn.fwd(qb, qb, qb)
+
+
+def test_causal_work_items_and_kv_tile_counts(lib):
+    # top-left causal: Q tile t attends KV tiles 0..t (capped by the key count)
+    for B, H, Sq, Sk in ((1, 2, 1024, 1024), (2, 1, 640, 300), (1, 1, 300, 900)):
+        p = attn.plan(B, H, Sq, Sk, 128, num_sms=152, causal=True)
+        kv = -(-Sk // 128)
+        seen = {}
+        for item in range(p["work_items"]):
+            bh, qt0, n0, n1 = attn.work_item(item, B, H, Sq, Sk, causal=True)
+            seen[(bh, qt0)] = (n0, n1)
+            assert n0 == min(qt0 + 1, kv)
+            assert n1 == (min(qt0 + 2, kv) if qt0 + 1 < p["q_tiles"] else 0)
+        assert set(seen) == {(bh, 2 * i) for bh in range(B * H) for i in range(-(-p["q_tiles"] // 2))}
+        # pairs numbered from the last one down: heaviest first when Sq == Sk (even tile count)
+        work = [sum(attn.work_item(k, B, H, Sq, Sk, causal=True)[2:]) for k in range(p["work_items"])]
+        if Sq == Sk:
+            assert all(a >= b for a, b in zip(work, work[1:]))
+
+
+def test_schedule_covers_every_item_once(lib):
+    for items, grid in ((1024, 152), (1152, 152), (7, 152), (300, 16)):
+        for causal in (False, True):
+            got = []
+            for cta in range(grid):
+                r = 0
+                while True:
+                    k = attn.schedule(cta, r, grid, items, causal)
+                    if k < 0:
+                        break
+                    got.append(k)
+                    r += 1
+            assert sorted(got) == list(range(items))
+    # dense: static stride; causal: every other round reversed
+    assert [attn.schedule(0, r, 148, 2048) for r in range(3)] == [0, 148, 296]
+    assert [attn.schedule(0, r, 148, 2048, causal=True) for r in range(3)] == [0, 295, 296]
