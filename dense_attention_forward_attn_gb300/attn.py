@@ -23,6 +23,7 @@ ATTN_ERR_UNSUPPORTED = -2
 ATTN_ERR_ARCH = -3
 ATTN_ERR_CUDA = -4
 ATTN_FLAG_CAUSAL = 1
+ATTN_FLAG_BSHD = 2
 
 
 class AttnError(RuntimeError):
@@ -85,8 +86,10 @@ def status_string(status: int) -> str:
     return library().attn_status_string(int(status)).decode()
 
 
-def _flags(causal: bool) -> int:
-    return ATTN_FLAG_CAUSAL if causal else 0
+def _flags(causal: bool, layout: str = "bhsd") -> int:
+    if layout not in ("bhsd", "bshd"):
+        raise ValueError("layout must be 'bhsd' ([B,H,S,D]) or 'bshd' ([B,S,H,D])")
+    return (ATTN_FLAG_CAUSAL if causal else 0) | (ATTN_FLAG_BSHD if layout == "bshd" else 0)
 
 
 def plan(B: int, H: int, Sq: int, Sk: int, D: int = 128, num_sms: int = 0,
@@ -125,20 +128,34 @@ def device_status(clear: bool = False) -> int:
 def _check(t, name):
     import torch
     if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.dim() != 4:
-        raise TypeError(f"{name} must be a 4-D torch.bfloat16 tensor [B, H, S, D]")
+        raise TypeError(f"{name} must be a 4-D torch.bfloat16 tensor")
     if not t.is_contiguous():
-        raise ValueError(f"{name} must be contiguous ([B, H, S, D] row-major)")
+        raise ValueError(f"{name} must be contiguous (row-major)")
+
+
+def _dims(q, k, layout):
+    """(B, H, Sq, Sk, D) from q and k in the given layout."""
+    if layout == "bshd":
+        B, Sq, H, D = q.shape
+        return B, H, Sq, k.shape[1], D
+    B, H, Sq, D = q.shape
+    return B, H, Sq, k.shape[2], D
 
 
 def fwd_into(q, k, v, o, lse=None, scale: float | None = None, stream=None,
-             causal: bool = False) -> None:
-    """Device tensors only: write softmax(scale q k^T) v into `o` (and LSE into `lse`)."""
+             causal: bool = False, layout: str = "bhsd") -> None:
+    """Device tensors only: write softmax(scale q k^T) v into `o` (and LSE into `lse`).
+
+    layout "bhsd": q/o [B,H,Sq,D], k/v [B,H,Sk,D]; "bshd": q/o [B,Sq,H,D], k/v [B,Sk,H,D].
+    lse is [B,H,Sq] either way.
+    """
     import torch
+    flags = _flags(causal, layout)
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
         _check(t, n)
-    B, H, Sq, D = q.shape
-    Sk = k.shape[2]
-    if tuple(k.shape) != (B, H, Sk, D) or tuple(v.shape) != (B, H, Sk, D) or tuple(o.shape) != (B, H, Sq, D):
+    B, H, Sq, Sk, D = _dims(q, k, layout)
+    kv_shape = (B, Sk, H, D) if layout == "bshd" else (B, H, Sk, D)
+    if tuple(k.shape) != kv_shape or tuple(v.shape) != kv_shape or tuple(o.shape) != tuple(q.shape):
         raise ValueError("shape mismatch between q, k, v, o")
     if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Sq)
                             or not lse.is_contiguous()):
@@ -149,13 +166,15 @@ def fwd_into(q, k, v, o, lse=None, scale: float | None = None, stream=None,
         stream = torch.cuda.current_stream(q.device).cuda_stream
     rc = library().attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                lse.data_ptr() if lse is not None else None, B, H, Sq, Sk, D,
-                               float(scale), _flags(causal), stream)
+                               float(scale), flags, stream)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
 
 
-def fwd(q, k, v, scale: float | None = None, return_lse: bool = True, causal: bool = False):
-    """Attention forward.  q [B,H,Sq,D], k/v [B,H,Sk,D], BF16 contiguous.
+def fwd(q, k, v, scale: float | None = None, return_lse: bool = True, causal: bool = False,
+        layout: str = "bhsd"):
+    """Attention forward.  q [B,H,Sq,D], k/v [B,H,Sk,D] (or [B,S,H,D] with layout="bshd"),
+    BF16 contiguous.  Returns (o in q's layout, lse [B,H,Sq] or None).
 
     CUDA tensors: runs on the current stream, returns (o, lse) on the device.
     CPU tensors: copies the inputs to the current CUDA device (pinned host
@@ -168,10 +187,10 @@ def fwd(q, k, v, scale: float | None = None, return_lse: bool = True, causal: bo
     if host:
         dev = torch.device("cuda", torch.cuda.current_device())
         q, k, v = (t.pin_memory().to(dev, non_blocking=True) for t in (q, k, v))
-    B, H, Sq, D = q.shape
-    o = torch.empty((B, H, Sq, D), dtype=torch.bfloat16, device=q.device)
+    B, H, Sq, _, D = _dims(q, k, layout)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device) if return_lse else None
-    fwd_into(q, k, v, o, lse, scale, causal=causal)
+    fwd_into(q, k, v, o, lse, scale, causal=causal, layout=layout)
     if host:
         o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
         o_h.copy_(o, non_blocking=True)

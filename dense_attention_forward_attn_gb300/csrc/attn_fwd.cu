@@ -67,15 +67,27 @@ int device_info(int dev, DeviceInfo* out) {
   return ATTN_OK;
 }
 
-// [BH, S, 128] BF16 viewed as a 3-D tensor (128, S, BH); box 64 x 128 x 1, 128-byte swizzle.
-int encode_bhsd(CUtensorMap* map, const void* base, int64_t bh, int64_t s) {
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(attn::kHeadDim), static_cast<cuuint64_t>(s),
-                        static_cast<cuuint64_t>(bh)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(attn::kHeadDim) * 2,
-                           static_cast<cuuint64_t>(s) * attn::kHeadDim * 2};
-  cuuint32_t box[3] = {64, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+// A BF16 [B,H,S,128] tensor as the 3-D TMA tensor (128, S, B*H), or a [B,S,H,128] tensor as the
+// 4-D tensor (128, H, S, B).  Box: 64 columns x 128 sequence rows of one head, 128-byte swizzle,
+// L2 promotion 256 B.  Rows past the sequence end of a head read as zeros.
+int encode_qkv(CUtensorMap* map, const void* base, int64_t B, int64_t H, int64_t S, bool bshd) {
+  const cuuint64_t D = attn::kHeadDim, e = 2;
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4];
+  cuuint32_t rank;
+  if (bshd) {
+    rank = 4;
+    dims[0] = D; dims[1] = H; dims[2] = S; dims[3] = B;
+    strides[0] = D * e; strides[1] = H * D * e; strides[2] = S * H * D * e;
+    box[0] = 64; box[1] = 1; box[2] = 128; box[3] = 1;
+  } else {
+    rank = 3;
+    dims[0] = D; dims[1] = S; dims[2] = B * H;
+    strides[0] = D * e; strides[1] = S * D * e;
+    box[0] = 64; box[1] = 128; box[2] = 1;
+  }
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -205,14 +217,22 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
   if (rc != ATTN_OK) return rc;
 
   alignas(64) CUtensorMap tm_q, tm_k, tm_v;
-  if (encode_bhsd(&tm_q, q, bh, Sq) != ATTN_OK || encode_bhsd(&tm_k, k, bh, Sk) != ATTN_OK ||
-      encode_bhsd(&tm_v, v, bh, Sk) != ATTN_OK)
+  const bool bshd = (flags & ATTN_FLAG_BSHD) != 0;
+  if (encode_qkv(&tm_q, q, B, H, Sq, bshd) != ATTN_OK ||
+      encode_qkv(&tm_k, k, B, H, Sk, bshd) != ATTN_OK ||
+      encode_qkv(&tm_v, v, B, H, Sk, bshd) != ATTN_OK)
     return ATTN_ERR_CUDA;
 
   attn::Params p;
   p.o = o;
   p.lse = lse;
   p.sq = Sq;
+  p.heads = H;
+  p.bshd = bshd ? 1 : 0;
+  const int64_t Dl = attn::kHeadDim;
+  p.o_row_stride = bshd ? H * Dl : Dl;
+  p.o_head_stride = bshd ? Dl : static_cast<int64_t>(Sq) * Dl;
+  p.o_batch_stride = static_cast<int64_t>(H) * Sq * Dl;
   p.q_tiles = ceil_div(Sq, attn::kBlockM);
   p.kv_tiles = ceil_div(Sk, attn::kBlockN);
   p.kv_valid_last = Sk - (p.kv_tiles - 1) * attn::kBlockN;

@@ -71,8 +71,8 @@ constexpr int kMmaWarp = 13;
 // full 128-column score row; the correction and TMA/MMA roles work in 16-column chunks.
 #ifndef ATTN_REG_SOFTMAX
 #define ATTN_REG_SOFTMAX 200
-#define ATTN_REG_CORR 64
-#define ATTN_REG_MISC 48
+#define ATTN_REG_CORR 56
+#define ATTN_REG_MISC 56
 #endif
 constexpr uint32_t kRegSoftmax = ATTN_REG_SOFTMAX;
 constexpr uint32_t kRegCorr = ATTN_REG_CORR;
@@ -120,8 +120,13 @@ constexpr uint32_t kCtlOffset = (2 + kKvStages) * kTileBytes;
 constexpr uint32_t kSmemBytes = kCtlOffset + sizeof(SmemCtl) + 1024;   // +1 KiB for alignment
 
 struct Params {
-  void* o;          // BF16 [BH, Sq, 128]
-  float* lse;       // fp32 [BH, Sq] or null
+  void* o;          // BF16 output, [B,H,Sq,128] or [B,Sq,H,128] (strides below)
+  float* lse;       // fp32 [B,H,Sq] or null
+  int heads;        // H
+  int bshd;         // 1: Q/K/V/O are [B,S,H,D]; 0: [B,H,S,D]
+  int64_t o_row_stride;   // elements between consecutive query rows of one head
+  int64_t o_head_stride;  // elements between heads
+  int64_t o_batch_stride; // elements between batches
   int sq;
   int q_tiles;      // ceil(Sq / 128)
   int kv_tiles;     // ceil(Sk / 128)
@@ -264,13 +269,23 @@ __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const C
   uint32_t q_cnt[2] = {0, 0};  // Q loads issued per stage
   bool ok = true;
 
+  // Q/K/V tensor maps: 3-D (D, S, B*H) for [B,H,S,D] inputs, 4-D (D, H, S, B) for [B,S,H,D].
+  // A box is 64 columns x 128 rows of one head either way (the same swizzled SMEM tile).
+  auto load_box = [&](uint32_t dst, const CUtensorMap* tm, uint32_t fb, int col, int row, int bh) {
+    if (p.bshd) {
+      const int b = bh / p.heads, h = bh - b * p.heads;
+      ptx::tma_load_4d(dst, tm, fb, col, h, row, b);
+    } else {
+      ptx::tma_load_3d(dst, tm, fb, col, row, bh);
+    }
+  };
   auto load_kv = [&](const CUtensorMap* tm, int bh, int row) -> bool {
     if (!c.wait(ctl->kv_empty[slot], phase ^ 1u, kStatusTimeoutLoad)) return false;
     if (c.lane == 0) {
       const uint32_t fb = c.bar(ctl->kv_full[slot]);
       ptx::mbar_arrive_expect_tx(fb, kTileBytes);
-      ptx::tma_load_3d(c.skv(slot), tm, fb, 0, row, bh);
-      ptx::tma_load_3d(c.skv(slot) + kSlabBytes, tm, fb, 64, row, bh);
+      load_box(c.skv(slot), tm, fb, 0, row, bh);
+      load_box(c.skv(slot) + kSlabBytes, tm, fb, 64, row, bh);
     }
     __syncwarp();
     kv_used |= 1u << slot;
@@ -283,8 +298,8 @@ __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const C
     if (c.lane == 0) {
       const uint32_t fb = c.bar(ctl->q_full[q]);
       ptx::mbar_arrive_expect_tx(fb, kTileBytes);
-      ptx::tma_load_3d(c.sq(q), tm_q, fb, 0, row, bh);
-      ptx::tma_load_3d(c.sq(q) + kSlabBytes, tm_q, fb, 64, row, bh);
+      load_box(c.sq(q), tm_q, fb, 0, row, bh);
+      load_box(c.sq(q) + kSlabBytes, tm_q, fb, 64, row, bh);
     }
     __syncwarp();
     ++q_cnt[q];
@@ -606,7 +621,9 @@ __device__ __forceinline__ bool epilogue(const Ctx& c, const Params& p, int q, c
   const float inv_l = 1.0f / l;
   const int grow = (w.qt0 + q) * kBlockM + row;
   const bool store = grow < p.sq;   // rows past a ragged end of Q are computed but not stored
-  uint8_t* out = static_cast<uint8_t*>(p.o) + (static_cast<size_t>(w.bh) * p.sq + grow) * (kHeadDim * 2);
+  const int b = w.bh / p.heads, h = w.bh - b * p.heads;
+  uint8_t* out = static_cast<uint8_t*>(p.o) +
+                 (b * p.o_batch_stride + h * p.o_head_stride + grow * p.o_row_stride) * 2;
   const uint32_t taddr_o = c.tmem + (row_base << 16) + col_o(q);
 #pragma unroll 2
   for (int cc = 0; cc < 8; ++cc) {

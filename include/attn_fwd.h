@@ -74,12 +74,19 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 
 /* Flags of attn_fwd_ex. */
 #define ATTN_FLAG_CAUSAL 1 /* query i attends keys j <= i (top-left aligned, i and j from 0) */
-#define ATTN_FLAGS_ALL ATTN_FLAG_CAUSAL
+#define ATTN_FLAG_BSHD 2   /* q, k, v, o are [B, S, H, D] contiguous (lse stays [B, H, Sq]) */
+#define ATTN_FLAGS_ALL (ATTN_FLAG_CAUSAL | ATTN_FLAG_BSHD)
 
 /*
  * attn_fwd_ex -- attn_fwd with options.  Arguments, ownership, errors and
  * asynchrony as attn_fwd; flags is a bitwise OR of ATTN_FLAG_* (0 = attn_fwd),
  * other bits give ATTN_ERR_INVALID_ARG.
+ *
+ * ATTN_FLAG_BSHD: q is [B, Sq, H, D], k and v [B, Sk, H, D], o [B, Sq, H, D],
+ * all contiguous (the layout FlashAttention-4 is timed on: "B200 Attention
+ * Kernel from Scratch to Near-SOTA in 60 Diagrams", Appendix "Benchmark
+ * Calibration", the direct-BSHD variant); no conversion copies are made.
+ * lse stays [B, H, Sq].  Same alignment and overlap rules.
  *
  * ATTN_FLAG_CAUSAL: the causal mask, key j is used by query i only when
  * j <= i, i.e. the two sequences are aligned at their first positions; every

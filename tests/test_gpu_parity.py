@@ -264,3 +264,27 @@ def test_causal_full_size_sampled_rows(name):
     rows = np.concatenate([rng.integers(0, w.Sq, 300), [0, 127, w.Sq - 1]])
     o_ref, lse_ref = oracle.attn_fwd_rows(qb, kb, vb, w.scale, bh, rows, causal=True)
     _assert_close(o.reshape(-1, w.Sq, w.D)[bh, rows], o_ref, lse.reshape(-1, w.Sq)[bh, rows], lse_ref)
+
+
+# ------------------------------------------------------------- direct [B,S,H,D] layout
+
+@pytest.mark.parametrize("shape,causal", [
+    ((2, 3, 256, 384), False),
+    ((1, 4, 300, 300), True),
+    ((2, 2, 129, 1000), False),
+])
+def test_bshd_layout(shape, causal):
+    B, H, Sq, Sk = shape
+    qb, kb, vb = wl.make_inputs_bits(B, H, Sq, Sk, 128, seed=sum(shape))
+    scale = 1.0 / math.sqrt(128)
+    # the same tensors laid out [B,S,H,D]: the kernel reads them directly, no conversion copy
+    q, k, v = (wl.bits_to_torch(np.ascontiguousarray(x.transpose(0, 2, 1, 3))).cuda() for x in (qb, kb, vb))
+    o, lse = attn.fwd(q, k, v, scale=scale, causal=causal, layout="bshd")
+    torch.cuda.synchronize()
+    assert o.shape == (B, Sq, H, 128) and lse.shape == (B, H, Sq)
+    o_ref, lse_ref = oracle.attn_fwd(qb, kb, vb, scale, causal=causal)
+    o_bhsd = o.float().cpu().numpy().astype(np.float64).transpose(0, 2, 1, 3)
+    _assert_close(o_bhsd, o_ref, lse.cpu().numpy().astype(np.float64), lse_ref)
+    # bitwise equal to the [B,H,S,D] path on the same values
+    o2, lse2 = attn.fwd(*(wl.bits_to_torch(x).cuda() for x in (qb, kb, vb)), scale=scale, causal=causal)
+    assert torch.equal(o2, o.transpose(1, 2).contiguous()) and torch.equal(lse2, lse)

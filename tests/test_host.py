@@ -137,6 +137,17 @@ def test_argument_checks_before_any_cuda_call(lib):
     assert _call(lib, **base, lse=4 * big + 64) == attn.ATTN_ERR_INVALID_ARG       # lse inside o
 
 
+def test_flags_are_checked(lib):
+    big = 1 << 40
+    vp = ctypes.c_void_p
+    rc = lib.attn_fwd_ex(vp(big), vp(2 * big), vp(3 * big), vp(4 * big), None, 1, 1, 128, 128,
+                         128, 0.1, 4, None)
+    assert rc == attn.ATTN_ERR_INVALID_ARG
+    with pytest.raises(ValueError):
+        attn._flags(False, "sbhd")
+    assert attn._flags(True, "bshd") == attn.ATTN_FLAG_CAUSAL | attn.ATTN_FLAG_BSHD
+
+
 def test_empty_problems_are_ok_without_launch(lib):
     assert _call(lib, q=0, k=0, v=0, o=0, B=0) == attn.ATTN_OK
     assert _call(lib, q=0, k=0, v=0, o=0, H=0) == attn.ATTN_OK
