@@ -11,6 +11,7 @@ Functions
 attn_fwd        plain definition, every row            (parity pinned)
 attn_fwd_rows   plain definition, selected rows         (parity pinned: same C row routine)
 attn_probs      materialised softmax of one head        (parity pinned)
+attn_bwd        gradients dQ, dK, dV of the definition  (parity pinned)
 online.*        the pages' tiled online-softmax steps   (parity pinned, see online.py)
 
 What the plain definition is and where it comes from is stated in the header of
@@ -69,6 +70,9 @@ def _load():
             lib.oracle_attn_fwd_rows.restype = i32
             lib.oracle_attn_probs.argtypes = [vp, vp, i64, i64, i64, f64, i32, vp]
             lib.oracle_attn_probs.restype = i32
+            lib.oracle_attn_bwd.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, f64, i32,
+                                            vp, vp, vp, i32]
+            lib.oracle_attn_bwd.restype = i32
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = i32
             _lib = lib
@@ -143,3 +147,21 @@ def attn_probs(q_head, k_head, scale: float, causal: bool = False):
     if rc != 0:
         raise RuntimeError(f"oracle_attn_probs failed: {rc}")
     return p
+
+
+def attn_bwd(q, k, v, do, scale: float, causal: bool = False, nthreads: int = 0):
+    """(dQ [B,H,Sq,D], dK [B,H,Sk,D], dV [B,H,Sk,D]) in fp64 for upstream gradient do = dL/dO."""
+    q, k, v, do = _bits(q), _bits(k), _bits(v), _bits(do)
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    if k.shape != (B, H, Sk, D) or v.shape != (B, H, Sk, D) or do.shape != q.shape:
+        raise ValueError("shape mismatch")
+    dq = np.empty((B, H, Sq, D), dtype=np.float64)
+    dk = np.empty((B, H, Sk, D), dtype=np.float64)
+    dv = np.empty((B, H, Sk, D), dtype=np.float64)
+    rc = _load().oracle_attn_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, do.ctypes.data, B, H,
+                                 Sq, Sk, D, float(scale), int(bool(causal)), dq.ctypes.data,
+                                 dk.ctypes.data, dv.ctypes.data, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_bwd failed: {rc}")
+    return dq, dk, dv

@@ -201,3 +201,81 @@ int oracle_attn_probs(const uint16_t *q_head, const uint16_t *k_head,
     }
     return 0;
 }
+
+/*
+ * Backward of the same plain definition, for one loss L with dL/dO = dO given:
+ *     P     = softmax(scale * Q K^T)            (masked entries 0 when causal)
+ *     dV    = P^T dO
+ *     dP    = dO V^T
+ *     dS_ij = P_ij * (dP_ij - sum_k P_ik dP_ik)
+ *     dQ    = scale * dS K
+ *     dK    = scale * dS^T Q
+ * (the chain rule through O = P V and the softmax Jacobian; "Attention for
+ * sm90, Line by Line", the exp2 question, is where the pages make the LSE the
+ * forward's residual for this pass).  Row by row in fp64: p and dp of a query
+ * row are materialised (Sk doubles each), dQ_i is finished per row, dK and dV
+ * accumulate over rows.  Parallel over (b, h) only (dK/dV sum over rows).
+ * do_ is [B,H,Sq,D] BF16 bits; dq [B,H,Sq,D], dk and dv [B,H,Sk,D] fp64.
+ */
+int oracle_attn_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, const uint16_t *do_,
+                    int64_t B, int64_t H, int64_t Sq, int64_t Sk, int64_t D, double scale,
+                    int causal, double *dq, double *dk, double *dv, int nthreads)
+{
+    if (B < 0 || H < 0 || Sq < 0 || Sk <= 0 || D <= 0) return -1;
+    set_threads(nthreads);
+    const int64_t heads = B * H;
+    int err = 0;
+#pragma omp parallel
+    {
+        double *p = (double *)malloc((size_t)Sk * sizeof(double));
+        double *dp = (double *)malloc((size_t)Sk * sizeof(double));
+        if (!p || !dp) {
+#pragma omp atomic write
+            err = -2;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t bh = 0; bh < heads; ++bh) {
+            if (!p || !dp) continue;
+            const uint16_t *qh = q + bh * Sq * D, *kh = k + bh * Sk * D, *vh = v + bh * Sk * D;
+            const uint16_t *doh = do_ + bh * Sq * D;
+            double *dqh = dq + bh * Sq * D, *dkh = dk + bh * Sk * D, *dvh = dv + bh * Sk * D;
+            for (int64_t x = 0; x < Sk * D; ++x) { dkh[x] = 0.0; dvh[x] = 0.0; }
+            for (int64_t i = 0; i < Sq; ++i) {
+                const int64_t nk = keys_for_row(i, Sk, causal);
+                /* p_i: softmax of the scaled scores of row i */
+                double m = -INFINITY;
+                for (int64_t j = 0; j < nk; ++j) {
+                    double dot = 0.0;
+                    for (int64_t d = 0; d < D; ++d)
+                        dot += bf16_to_f64(qh[i * D + d]) * bf16_to_f64(kh[j * D + d]);
+                    p[j] = scale * dot;
+                    if (p[j] > m) m = p[j];
+                }
+                double l = 0.0;
+                for (int64_t j = 0; j < nk; ++j) { p[j] = exp(p[j] - m); l += p[j]; }
+                for (int64_t j = 0; j < nk; ++j) p[j] /= l;
+                /* dp_i = dO_i V^T, delta_i = sum_j p_ij dp_ij */
+                double delta = 0.0;
+                for (int64_t j = 0; j < nk; ++j) {
+                    double dot = 0.0;
+                    for (int64_t d = 0; d < D; ++d)
+                        dot += bf16_to_f64(doh[i * D + d]) * bf16_to_f64(vh[j * D + d]);
+                    dp[j] = dot;
+                    delta += p[j] * dot;
+                }
+                for (int64_t d = 0; d < D; ++d) dqh[i * D + d] = 0.0;
+                for (int64_t j = 0; j < nk; ++j) {
+                    const double ds = p[j] * (dp[j] - delta);
+                    for (int64_t d = 0; d < D; ++d) {
+                        dqh[i * D + d] += scale * ds * bf16_to_f64(kh[j * D + d]);
+                        dkh[j * D + d] += scale * ds * bf16_to_f64(qh[i * D + d]);
+                        dvh[j * D + d] += p[j] * bf16_to_f64(doh[i * D + d]);
+                    }
+                }
+            }
+        }
+        free(p);
+        free(dp);
+    }
+    return err;
+}

@@ -319,3 +319,70 @@ def test_causal_closed_forms():
     np.testing.assert_allclose(p.sum(axis=1), 1.0, atol=1e-14)
     o_r, l_r = oracle.attn_fwd_rows(qb, kb, vb, 0.4, [0, 1, 1], [0, 7, 49], causal=True)
     np.testing.assert_array_equal(o_r, o_c.reshape(2, 50, 16)[[0, 1, 1], [0, 7, 49]])
+
+
+# ---------------------------------------------------------------- backward
+
+def _autograd_f64(qb, kb, vb, dob, scale, causal):
+    q, k, v = (_f64(x).requires_grad_(True) for x in (qb, kb, vb))
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, scale=scale, is_causal=causal)
+    o.backward(_f64(dob))
+    return q.grad.numpy(), k.grad.numpy(), v.grad.numpy()
+
+
+@pytest.mark.parametrize("shape,causal", [((1, 2, 48, 64, 32), False), ((2, 1, 40, 24, 16), True),
+                                          ((1, 1, 30, 90, 16), True), ((1, 2, 128, 128, 128), False)])
+def test_backward_oracle_matches_autograd_f64(shape, causal):
+    B, H, Sq, Sk, D = shape
+    qb, kb, vb = wl.make_inputs_bits(B, H, Sq, Sk, D, seed=41)
+    dob = wl.make_inputs_bits(B, H, Sq, Sq, D, seed=42)[0]
+    scale = 1.0 / math.sqrt(D)
+    got = oracle.attn_bwd(qb, kb, vb, dob, scale, causal=causal)
+    ref = _autograd_f64(qb, kb, vb, dob, scale, causal)
+    for g, r in zip(got, ref):
+        np.testing.assert_allclose(g, r, rtol=1e-9, atol=1e-12)
+
+
+def test_backward_oracle_matches_central_differences():
+    # dL/dx for L = sum(O * dO) by central differences of the oracle's own forward, on a
+    # handful of entries of each input (fp64 forward through a perturbed fp64 copy).
+    B, H, Sq, Sk, D = 1, 1, 6, 5, 4
+    qb, kb, vb = wl.make_inputs_bits(B, H, Sq, Sk, D, seed=43, qk_std=1.5)
+    dob = wl.make_inputs_bits(B, H, Sq, Sq, D, seed=44)[0]
+    scale = 0.7
+    for causal in (False, True):
+        dq, dk, dv = oracle.attn_bwd(qb, kb, vb, dob, scale, causal=causal)
+        q, k, v, do = (online.bf16_bits_to_f64(x)[0, 0] for x in (qb, kb, vb, dob))
+
+        def loss(q_, k_, v_):
+            s = scale * q_ @ k_.T
+            if causal:
+                s = np.where(np.tril(np.ones((Sq, Sk), bool)), s, -np.inf)
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            p /= p.sum(axis=1, keepdims=True)
+            return float(((p @ v_) * do).sum())
+
+        h = 1e-6
+        for which, grad in (("q", dq), ("k", dk), ("v", dv)):
+            for (r, d) in ((0, 0), (2, 3), (4, 1)):
+                args = {"q": q.copy(), "k": k.copy(), "v": v.copy()}
+                args[which][r, d] += h
+                lp = loss(args["q"], args["k"], args["v"])
+                args[which][r, d] -= 2 * h
+                lm = loss(args["q"], args["k"], args["v"])
+                assert abs((lp - lm) / (2 * h) - grad[0, 0, r, d]) <= 1e-7, (which, r, d, causal)
+
+
+def test_backward_closed_forms():
+    qb, kb, vb = wl.make_inputs_bits(1, 2, 20, 30, 16, seed=45)
+    dob = wl.make_inputs_bits(1, 2, 20, 20, 16, seed=46)[0]
+    dq, dk, dv = oracle.attn_bwd(qb, kb, vb, dob, 0.3)
+    # sum_j dS_ij = 0 for every row, so dK summed over keys is 0 and dQ is orthogonal to a
+    # common shift of all keys; dV summed over keys equals dO summed over queries.
+    np.testing.assert_allclose(dk.sum(axis=2), 0.0, atol=1e-12)
+    do = online.bf16_bits_to_f64(dob)
+    np.testing.assert_allclose(dv.sum(axis=2), do.sum(axis=2), rtol=1e-12, atol=1e-12)
+    # zero upstream gradient gives zero gradients
+    z = np.zeros_like(dob)
+    for g in oracle.attn_bwd(qb, kb, vb, z, 0.3):
+        assert not g.any()
