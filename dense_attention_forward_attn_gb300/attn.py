@@ -38,8 +38,8 @@ class _Plan(ctypes.Structure):
                 ("smem_bytes", ctypes.c_int), ("tmem_cols", ctypes.c_int)]
 
 
-EXPORTS = ("attn_fwd", "attn_fwd_ex", "attn_status_string", "attn_fwd_plan", "attn_fwd_work_item",
-           "attn_fwd_schedule", "attn_device_status")
+EXPORTS = ("attn_fwd", "attn_fwd_ex", "attn_bwd", "attn_status_string", "attn_fwd_plan",
+           "attn_fwd_work_item", "attn_fwd_schedule", "attn_device_status")
 
 
 def lib_path() -> str:
@@ -52,6 +52,9 @@ def _bind(lib):
     lib.attn_fwd.restype = i32
     lib.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp]
     lib.attn_fwd_ex.restype = i32
+    lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32,
+                             i32, vp]
+    lib.attn_bwd.restype = i32
     lib.attn_status_string.argtypes = [i32]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_fwd_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(_Plan)]
@@ -201,3 +204,31 @@ def fwd(q, k, v, scale: float | None = None, return_lse: bool = True, causal: bo
         torch.cuda.current_stream().synchronize()
         return o_h, lse_h
     return o, lse
+
+
+def bwd(q, k, v, o, dout, lse, scale: float | None = None, causal: bool = False):
+    """Backward of fwd (device tensors, [B,H,S,D] BF16; lse [B,H,Sq] fp32 from fwd).
+
+    Returns (dq, dk, dv), BF16 in the shapes of q, k, v.  Runs on the current stream.
+    """
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _check(t, n)
+    B, H, Sq, Sk, D = _dims(q, k, "bhsd")
+    if tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
+        raise ValueError("o and dout must have q's shape")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Sq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 tensor [B, H, Sq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    delta = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = library().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                            delta.data_ptr(), B, H, Sq, Sk, D, float(scale), _flags(causal), stream)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd")
+    return dq, dk, dv

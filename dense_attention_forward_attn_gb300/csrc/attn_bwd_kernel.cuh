@@ -1,0 +1,552 @@
+// attn_bwd_kernel.cuh -- backward of the dense head_dim-128 attention for sm_103a, consuming
+// the forward's natural-log LSE ("Attention for sm90, Line by Line", the exp2 question: the
+// residual is the row max in natural-log units so the backward can rebuild P).
+//
+// With P = exp(scale * Q K^T - LSE) (masked entries 0), dO = dL/dO and
+//     delta_i = sum_d dO_id O_id,   dS = P o (dO V^T - delta),
+//     dV = P^T dO,   dK = scale * dS^T Q,   dQ = scale * dS K,
+// three kernels run in order on one stream:
+//   attn_bwd_delta_kernel  delta (fp32, one warp per query row)
+//   attn_bwd_dkdv_kernel   one CTA per 128-row K/V tile: S^T = K Q^T and dP^T = V dO^T into
+//                          TMEM, P^T and dS^T (BF16) written back over their upper halves, then
+//                          dV += P^T dO and dK += dS^T Q with A from TMEM; loops over Q tiles
+//   attn_bwd_dq_kernel     one CTA per 128-row Q tile: S = Q K^T and dP = dO V^T, dS (BF16)
+//                          over S, dQ += dS K; loops over K/V tiles
+// Every gradient is written by exactly one CTA (no atomics: deterministic).  dQ repeats the
+// S and dP products of dK/dV (7 tile products per tile pair instead of 5).
+//
+// Roles per CTA (192 threads): warps 0-3 an elementwise warpgroup (one TMEM lane = one row per
+// thread), warp 4 TMA, warp 5 tcgen05.mma issue and TMEM allocation.  Tiles are staged by TMA
+// with 128-byte swizzle exactly as in the forward kernel; every mbarrier wait is bounded.
+#pragma once
+#include <cuda.h>
+#include <cstdint>
+
+#include "attn_fwd_kernel.cuh"
+
+namespace attn {
+namespace bwd {
+
+constexpr int kThreads = 192;
+constexpr int kLoadWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kRing = 4;   // K/V (dQ kernel) or Q/dO (dK/dV kernel) tiles in flight
+
+struct Params {
+  const void* lse;     // fp32 [B,H,Sq], natural log (the forward's output)
+  float* delta;        // fp32 [B,H,Sq]
+  void* out0;          // dQ kernel: dQ; dK/dV kernel: dK        BF16 [B,H,S,128]
+  void* out1;          // dK/dV kernel: dV
+  int sq, sk;
+  int q_tiles, kv_tiles;
+  int q_valid_last, kv_valid_last;   // valid rows in the last Q / K/V tile, 1..128
+  int bh;
+  int causal;
+  float scale;         // softmax scale
+  float scale_log2;    // scale * log2(e)
+};
+
+struct alignas(8) SmemCtl {
+  uint64_t fixed_full;          // the CTA's own two resident tiles are in SMEM
+  uint64_t ring_full[kRing], ring_empty[kRing];
+  uint64_t mma_full;            // MMA -> elementwise: the two score-like tiles are in TMEM
+  uint64_t ew_full;             // elementwise -> MMA: BF16 operands written into TMEM
+  uint64_t acc_full;            // MMA -> elementwise: the accumulators are final
+  uint64_t vec_sync;            // elementwise warps exchanged per-column vectors (dK/dV)
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort_flag;
+  float lse2[2][kBlockM];       // dK/dV kernel: LSE * log2(e) of the current Q tile's columns
+  float dlt[2][kBlockM];        // dK/dV kernel: delta of the current Q tile's columns
+};
+
+constexpr uint32_t kCtlOffset = (2 + kRing) * kTileBytes;
+constexpr uint32_t kSmemBytes = kCtlOffset + sizeof(SmemCtl) + 1024;
+
+// Bounded waits, as in the forward kernel: all 32 lanes call; false = timed out or aborted.
+struct Sync {
+  SmemCtl* ctl;
+  uint32_t lane;
+  __device__ uint32_t bar(const uint64_t& b) const { return ptx::smem_u32(&b); }
+  __device__ bool wait(const uint64_t& b, uint32_t parity, unsigned role_bit) const {
+    const uint32_t addr = bar(b);
+    if (__all_sync(0xffffffffu, ptx::mbar_try_wait(addr, parity))) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (true) {
+      if (__all_sync(0xffffffffu, ptx::mbar_try_wait(addr, parity))) return true;
+      const bool stop = ctl->abort_flag != 0 || (ptx::globaltimer_ns() - t0) > kWaitLimitNs;
+      if (__any_sync(0xffffffffu, stop)) {
+        if (lane == 0) {
+          ctl->abort_flag = 1;
+          atomicOr(&g_attn_status, role_bit);
+        }
+        __syncwarp();
+        return false;
+      }
+    }
+  }
+  __device__ void drain_wait(const uint64_t& b, uint32_t parity) const {
+    const uint32_t addr = bar(b);
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!__all_sync(0xffffffffu, ptx::mbar_try_wait(addr, parity))) {
+      if (__any_sync(0xffffffffu, (ptx::globaltimer_ns() - t0) > kDrainLimitNs)) {
+        if (lane == 0) atomicOr(&g_attn_status, kStatusTimeoutDrain);
+        return;
+      }
+    }
+  }
+  __device__ void arrive(const uint64_t& b) const {
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bar(b));
+  }
+};
+
+// ------------------------------------------------------------------ delta = rowsum(dO o O)
+__global__ void __launch_bounds__(256) attn_bwd_delta_kernel(const uint16_t* __restrict__ o,
+                                                             const uint16_t* __restrict__ dout,
+                                                             float* __restrict__ delta,
+                                                             int64_t rows) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const uint32_t lane = threadIdx.x & 31u;
+  if (row >= rows) return;
+  const uint2 a = *reinterpret_cast<const uint2*>(o + row * kHeadDim + lane * 4);
+  const uint2 b = *reinterpret_cast<const uint2*>(dout + row * kHeadDim + lane * 4);
+  auto lo = [](uint32_t x) { return __uint_as_float(x << 16); };
+  auto hi = [](uint32_t x) { return __uint_as_float(x & 0xffff0000u); };
+  float acc = lo(a.x) * lo(b.x);
+  acc = fmaf(hi(a.x), hi(b.x), acc);
+  acc = fmaf(lo(a.y), lo(b.y), acc);
+  acc = fmaf(hi(a.y), hi(b.y), acc);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) delta[row] = acc;
+}
+
+// ------------------------------------------------------------------ shared pieces
+// D[tmem cols d] (+)= A[smem, K-major SW128] * B[smem, K-major SW128]^T, 128x128x128.
+__device__ __forceinline__ void mma_kmajor(uint32_t d, uint32_t a_smem, uint32_t b_smem) {
+  constexpr uint32_t idesc = make_idesc_bf16(128, 128, 0);
+  const uint64_t a0 = smem_desc_sw128(a_smem, 16, 1024);
+  const uint64_t b0 = smem_desc_sw128(b_smem, 16, 1024);
+#pragma unroll
+  for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+    const uint32_t off16 = ((kk >> 2) * kSlabBytes + (kk & 3) * 32) >> 4;
+    ptx::mma_ss(d, a0 + off16, b0 + off16, idesc, kk > 0);
+  }
+}
+
+// D[tmem cols d] (+)= A[tmem cols a, packed BF16 128x128] * B[smem 128 rows x 128, MN-major].
+__device__ __forceinline__ void mma_tmem_a(uint32_t d, uint32_t a, uint32_t b_smem,
+                                           bool accumulate) {
+  constexpr uint32_t idesc = make_idesc_bf16(128, 128, 1);
+  const uint64_t b0 = smem_desc_sw128(b_smem, kSlabBytes, 1024);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    ptx::mma_ts(d, a + kk * 8, b0 + ((kk * 16 * 128) >> 4), idesc,
+                (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// Load two 64-column boxes (one 128-row tile) of a [B*H, S, 128] tensor map.
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* tm, uint32_t bar,
+                                          int row, int bh) {
+  ptx::tma_load_3d(dst, tm, bar, 0, row, bh);
+  ptx::tma_load_3d(dst + kSlabBytes, tm, bar, 64, row, bh);
+}
+
+// Write 16 fp32 accumulator columns as BF16 (times `mul`) to a global row.
+__device__ __forceinline__ void store_cols16(uint8_t* out, const uint32_t (&r)[16], float mul) {
+  uint32_t pk[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+  ptx::st_global_v4(out, pk[0], pk[1], pk[2], pk[3]);
+  ptx::st_global_v4(out + 16, pk[4], pk[5], pk[6], pk[7]);
+}
+
+__device__ __forceinline__ void zero_row(uint8_t* out) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) ptx::st_global_v4(out + 16 * i, 0u, 0u, 0u, 0u);
+}
+
+struct Layout {
+  SmemCtl* ctl;
+  uint32_t base;   // 1024-aligned shared address of the first resident tile
+  __device__ uint32_t fixed(int i) const { return base + i * kTileBytes; }
+  __device__ uint32_t ring(int s) const { return base + (2 + s) * kTileBytes; }
+};
+
+__device__ __forceinline__ Layout setup(uint8_t* smem_raw) {
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  Layout L;
+  L.base = (raw + 1023u) & ~1023u;
+  L.ctl = reinterpret_cast<SmemCtl*>(smem_raw + (L.base - raw) + kCtlOffset);
+  return L;
+}
+
+__device__ __forceinline__ void init_barriers(SmemCtl* ctl, const Sync& s) {
+  ptx::mbar_init(s.bar(ctl->fixed_full), 1);
+  for (int i = 0; i < kRing; ++i) {
+    ptx::mbar_init(s.bar(ctl->ring_full[i]), 1);
+    ptx::mbar_init(s.bar(ctl->ring_empty[i]), 1);
+  }
+  ptx::mbar_init(s.bar(ctl->mma_full), 1);
+  ptx::mbar_init(s.bar(ctl->ew_full), 4);
+  ptx::mbar_init(s.bar(ctl->acc_full), 1);
+  ptx::mbar_init(s.bar(ctl->vec_sync), 4);
+  ptx::mbar_init(s.bar(ctl->drain), 1);
+  ctl->abort_flag = 0;
+  ptx::fence_mbar_init();
+}
+
+// TMA warp: the two resident tiles, then `n` pairs of streamed tiles (first map, second map)
+// for tile indices t0 .. t0+n-1, through the ring.
+__device__ __forceinline__ void stream_tiles(const Layout& L, const Sync& s, const CUtensorMap* f0,
+                                             const CUtensorMap* f1, int frow, const CUtensorMap* r0,
+                                             const CUtensorMap* r1, int t0, int n, int bh) {
+  SmemCtl* ctl = L.ctl;
+  if (s.lane == 0) {
+    const uint32_t fb = s.bar(ctl->fixed_full);
+    ptx::mbar_arrive_expect_tx(fb, 2 * kTileBytes);
+    load_tile(L.fixed(0), f0, fb, frow, bh);
+    load_tile(L.fixed(1), f1, fb, frow, bh);
+  }
+  __syncwarp();
+  int slot = 0;
+  uint32_t phase = 0, used = 0, last_par = 0;
+  bool ok = true;
+  for (int t = 0; ok && t < 2 * n; ++t) {
+    if (!(ok = s.wait(ctl->ring_empty[slot], phase ^ 1u, kStatusTimeoutLoad))) break;
+    if (s.lane == 0) {
+      const uint32_t fb = s.bar(ctl->ring_full[slot]);
+      ptx::mbar_arrive_expect_tx(fb, kTileBytes);
+      load_tile(L.ring(slot), (t & 1) ? r1 : r0, fb, (t0 + (t >> 1)) * kBlockM, bh);
+    }
+    __syncwarp();
+    used |= 1u << slot;
+    last_par = (last_par & ~(1u << slot)) | (phase << slot);
+    if (++slot == kRing) { slot = 0; phase ^= 1u; }
+  }
+  if (!ok) {
+    for (int i = 0; i < kRing; ++i)
+      if ((used >> i) & 1u) s.drain_wait(ctl->ring_full[i], (last_par >> i) & 1u);
+  }
+  s.drain_wait(ctl->fixed_full, 0);
+}
+
+// ------------------------------------------------------------------ dQ kernel
+// TMEM: S [0,128) with packed BF16 dS over columns 64..127, dP [128,256), dQ [256,384).
+constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+
+__device__ __forceinline__ void dq_item(const Params& p, int& bh, int& qt, int& nkv) {
+  if (p.causal) {   // heaviest Q tiles first
+    qt = p.q_tiles - 1 - static_cast<int>(blockIdx.x) / p.bh;
+    bh = static_cast<int>(blockIdx.x) % p.bh;
+    nkv = qt + 1 < p.kv_tiles ? qt + 1 : p.kv_tiles;
+  } else {
+    bh = static_cast<int>(blockIdx.x) / p.q_tiles;
+    qt = static_cast<int>(blockIdx.x) % p.q_tiles;
+    nkv = p.kv_tiles;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                   const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const Layout L = setup(smem_raw);
+  SmemCtl* ctl = L.ctl;
+  const uint32_t warp = threadIdx.x >> 5;
+  Sync s{ctl, threadIdx.x & 31u};
+  int bh, qt, nkv;
+  dq_item(p, bh, qt, nkv);
+
+  if (threadIdx.x == 0) init_barriers(ctl, s);
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(&ctl->tmem_base), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_alloc_base = ctl->tmem_base;
+  const bool tmem_ok = tmem_alloc_base == kTmemBase;
+  if (!tmem_ok && threadIdx.x == 0) atomicOr(&g_attn_status, kStatusTmemBase);
+
+  if (tmem_ok && warp == kLoadWarp) {
+    // resident: Q, dO of this tile; streamed: K_j, V_j
+    stream_tiles(L, s, &tm_q, &tm_do, qt * kBlockM, &tm_k, &tm_v, 0, nkv, bh);
+  } else if (tmem_ok && warp == kMmaWarp) {
+    const bool leader = ptx::elect_one();
+    bool ok = s.wait(ctl->fixed_full, 0, kStatusTimeoutMma);
+    int slot = 0;
+    uint32_t phase = 0;
+    for (int j = 0; ok && j < nkv; ++j) {
+      const int ks = slot;
+      if (!(ok = s.wait(ctl->ring_full[ks], phase, kStatusTimeoutMma))) break;
+      if (++slot == kRing) { slot = 0; phase ^= 1u; }
+      const int vs = slot;
+      if (!(ok = s.wait(ctl->ring_full[vs], phase, kStatusTimeoutMma))) break;
+      if (++slot == kRing) { slot = 0; phase ^= 1u; }
+      ptx::tc_fence_after();
+      if (leader) {
+        mma_kmajor(kTmemBase + kColS, L.fixed(0), L.ring(ks));    // S = Q K^T
+        mma_kmajor(kTmemBase + kColDP, L.fixed(1), L.ring(vs));   // dP = dO V^T
+        ptx::mma_commit(s.bar(ctl->mma_full));
+        ptx::mma_commit(s.bar(ctl->ring_empty[vs]));
+      }
+      __syncwarp();
+      if (!(ok = s.wait(ctl->ew_full, j & 1u, kStatusTimeoutMma))) break;
+      ptx::tc_fence_after();
+      if (leader) {
+        mma_tmem_a(kTmemBase + kColDQ, kTmemBase + kColS + kColP, L.ring(ks), j > 0);  // dQ += dS K
+        ptx::mma_commit(s.bar(ctl->ring_empty[ks]));
+        if (j == nkv - 1) ptx::mma_commit(s.bar(ctl->acc_full));
+      }
+      __syncwarp();
+    }
+    if (leader) ptx::mma_commit(s.bar(ctl->drain));
+    __syncwarp();
+    s.drain_wait(ctl->drain, 0);
+  } else if (tmem_ok && warp < 4) {
+    const uint32_t row_base = 32u * warp;
+    const int r = static_cast<int>(row_base + s.lane);
+    const int qrow = qt * kBlockM + r;
+    const bool row_ok = qrow < p.sq;
+    const size_t gi = static_cast<size_t>(bh) * p.sq + qrow;
+    const float lse2 = row_ok ? static_cast<const float*>(p.lse)[gi] * 1.4426950408889634f : 0.f;
+    const float dlt = row_ok ? p.delta[gi] : 0.f;
+    const uint32_t lane_off = row_base << 16;
+    bool ok = true;
+    for (int j = 0; ok && j < nkv; ++j) {
+      if (!(ok = s.wait(ctl->mma_full, j & 1u, kStatusTimeoutSoftmax))) break;
+      ptx::tc_fence_after();
+      int valid = kBlockN;
+      if (j == p.kv_tiles - 1) valid = p.kv_valid_last;
+      if (p.causal && j == qt) valid = min(valid, r + 1);
+      // high chunk first: the packed dS of chunk c lands on S columns 64+16c.., already read
+#pragma unroll
+      for (int c = 3; c >= 0; --c) {
+        uint32_t sr[32], dr[32];
+        ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColS + 32 * c, sr);
+        ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColDP + 32 * c, dr);
+        ptx::tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float ds[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int col = 32 * c + 2 * i + h;
+            const float pv = ptx::ex2_ftz(fmaf(__uint_as_float(sr[2 * i + h]), p.scale_log2, -lse2));
+            ds[h] = col < valid ? pv * (__uint_as_float(dr[2 * i + h]) - dlt) : 0.f;
+          }
+          pk[i] = ptx::pack_bf16x2(ds[0], ds[1]);
+        }
+        ptx::tmem_st_32x32b_x16(kTmemBase + lane_off + kColS + kColP + 16 * c, pk);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      s.arrive(ctl->ew_full);
+    }
+    if (ok && s.wait(ctl->acc_full, 0, kStatusTimeoutSoftmax)) {
+      ptx::tc_fence_after();
+      uint8_t* out = static_cast<uint8_t*>(p.out0) + gi * (kHeadDim * 2);
+#pragma unroll 2
+      for (int c = 0; c < 8; ++c) {
+        uint32_t acc[16];
+        ptx::tmem_ld_32x32b_x16(kTmemBase + lane_off + kColDQ + 16 * c, acc);
+        ptx::tmem_wait_ld();
+        if (row_ok) store_cols16(out + 32 * c, acc, p.scale);
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_alloc_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ dK/dV kernel
+// TMEM: S^T [0,128) with packed BF16 P^T over 64..127, dP^T [128,256) with packed BF16 dS^T over
+// 192..255, dK [256,384), dV [384,512).
+constexpr uint32_t kColST = 0, kColDPT = 128, kColDK = 256, kColDV = 384;
+
+__device__ __forceinline__ void dkdv_item(const Params& p, int& bh, int& kt, int& q0, int& nq) {
+  if (p.causal) {   // heaviest K/V tiles (earliest keys) first
+    kt = static_cast<int>(blockIdx.x) / p.bh;
+    bh = static_cast<int>(blockIdx.x) % p.bh;
+    q0 = kt;        // Q tiles kt.. see keys of K/V tile kt (top-left alignment)
+    nq = kt < p.q_tiles ? p.q_tiles - kt : 0;
+  } else {
+    bh = static_cast<int>(blockIdx.x) / p.kv_tiles;
+    kt = static_cast<int>(blockIdx.x) % p.kv_tiles;
+    q0 = 0;
+    nq = p.q_tiles;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const Layout L = setup(smem_raw);
+  SmemCtl* ctl = L.ctl;
+  const uint32_t warp = threadIdx.x >> 5;
+  Sync s{ctl, threadIdx.x & 31u};
+  int bh, kt, q0, nq;
+  dkdv_item(p, bh, kt, q0, nq);
+
+  if (threadIdx.x == 0) init_barriers(ctl, s);
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(&ctl->tmem_base), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_alloc_base = ctl->tmem_base;
+  const bool tmem_ok = tmem_alloc_base == kTmemBase;
+  if (!tmem_ok && threadIdx.x == 0) atomicOr(&g_attn_status, kStatusTmemBase);
+
+  if (tmem_ok && warp == kLoadWarp && nq > 0) {
+    // resident: K, V of this tile; streamed: Q_i, dO_i
+    stream_tiles(L, s, &tm_k, &tm_v, kt * kBlockN, &tm_q, &tm_do, q0, nq, bh);
+  } else if (tmem_ok && warp == kMmaWarp && nq > 0) {
+    const bool leader = ptx::elect_one();
+    bool ok = s.wait(ctl->fixed_full, 0, kStatusTimeoutMma);
+    int slot = 0;
+    uint32_t phase = 0;
+    for (int i = 0; ok && i < nq; ++i) {
+      const int qs = slot;
+      if (!(ok = s.wait(ctl->ring_full[qs], phase, kStatusTimeoutMma))) break;
+      if (++slot == kRing) { slot = 0; phase ^= 1u; }
+      const int ds = slot;
+      if (!(ok = s.wait(ctl->ring_full[ds], phase, kStatusTimeoutMma))) break;
+      if (++slot == kRing) { slot = 0; phase ^= 1u; }
+      ptx::tc_fence_after();
+      if (leader) {
+        mma_kmajor(kTmemBase + kColST, L.fixed(0), L.ring(qs));    // S^T = K Q^T
+        mma_kmajor(kTmemBase + kColDPT, L.fixed(1), L.ring(ds));   // dP^T = V dO^T
+        ptx::mma_commit(s.bar(ctl->mma_full));
+      }
+      __syncwarp();
+      if (!(ok = s.wait(ctl->ew_full, i & 1u, kStatusTimeoutMma))) break;
+      ptx::tc_fence_after();
+      if (leader) {
+        mma_tmem_a(kTmemBase + kColDV, kTmemBase + kColST + kColP, L.ring(ds), i > 0);   // dV += P^T dO
+        mma_tmem_a(kTmemBase + kColDK, kTmemBase + kColDPT + kColP, L.ring(qs), i > 0);  // dK += dS^T Q
+        ptx::mma_commit(s.bar(ctl->ring_empty[qs]));
+        ptx::mma_commit(s.bar(ctl->ring_empty[ds]));
+        if (i == nq - 1) ptx::mma_commit(s.bar(ctl->acc_full));
+      }
+      __syncwarp();
+    }
+    if (leader) ptx::mma_commit(s.bar(ctl->drain));
+    __syncwarp();
+    s.drain_wait(ctl->drain, 0);
+  } else if (tmem_ok && warp < 4) {
+    const uint32_t row_base = 32u * warp;
+    const int r = static_cast<int>(row_base + s.lane);   // key row within the tile
+    const int krow = kt * kBlockN + r;
+    const uint32_t lane_off = row_base << 16;
+    const float* lse = static_cast<const float*>(p.lse) + static_cast<size_t>(bh) * p.sq;
+    const float* dl = p.delta + static_cast<size_t>(bh) * p.sq;
+    // Column vectors (LSE*log2 e, delta) of Q tile i, staged by all 128 threads; masked query
+    // columns (past Sq) get LSE = +inf, so P = 0 there.
+    auto fetch = [&](int i, float& a, float& d) {
+      const int qi = (q0 + i) * kBlockM + r;
+      a = qi < p.sq ? lse[qi] * 1.4426950408889634f : __int_as_float(0x7f800000);
+      d = qi < p.sq ? dl[qi] : 0.f;
+    };
+    bool ok = true;
+    float na = 0.f, nd = 0.f;
+    if (nq > 0) {
+      fetch(0, na, nd);
+      ctl->lse2[0][r] = na;
+      ctl->dlt[0][r] = nd;
+      s.arrive(ctl->vec_sync);
+    }
+    for (int i = 0; ok && i < nq; ++i) {
+      const int par = i & 1;
+      if (i + 1 < nq) fetch(i + 1, na, nd);   // next tile's vectors, in flight meanwhile
+      if (!(ok = s.wait(ctl->vec_sync, par, kStatusTimeoutSoftmax))) break;
+      if (!(ok = s.wait(ctl->mma_full, par, kStatusTimeoutSoftmax))) break;
+      ptx::tc_fence_after();
+      const bool diag = p.causal && q0 + i == kt;   // query column c < key row r is masked
+      const float* va = ctl->lse2[par];
+      const float* vd = ctl->dlt[par];
+#pragma unroll
+      for (int c = 3; c >= 0; --c) {
+        uint32_t sr[32], dr[32];
+        ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColST + 32 * c, sr);
+        ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColDPT + 32 * c, dr);
+        ptx::tmem_wait_ld();
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int i2 = 0; i2 < 16; ++i2) {
+          const int col = 32 * c + 2 * i2;
+          const float2 a = *reinterpret_cast<const float2*>(va + col);
+          const float2 d = *reinterpret_cast<const float2*>(vd + col);
+          float p0 = ptx::ex2_ftz(fmaf(__uint_as_float(sr[2 * i2]), p.scale_log2, -a.x));
+          float p1 = ptx::ex2_ftz(fmaf(__uint_as_float(sr[2 * i2 + 1]), p.scale_log2, -a.y));
+          if (diag) {
+            p0 = col < r ? 0.f : p0;
+            p1 = col + 1 < r ? 0.f : p1;
+          }
+          pp[i2] = ptx::pack_bf16x2(p0, p1);
+          pd[i2] = ptx::pack_bf16x2(p0 * (__uint_as_float(dr[2 * i2]) - d.x),
+                                    p1 * (__uint_as_float(dr[2 * i2 + 1]) - d.y));
+        }
+        ptx::tmem_st_32x32b_x16(kTmemBase + lane_off + kColST + kColP + 16 * c, pp);
+        ptx::tmem_st_32x32b_x16(kTmemBase + lane_off + kColDPT + kColP + 16 * c, pd);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      s.arrive(ctl->ew_full);
+      if (i + 1 < nq) {
+        // the other buffer was last read at tile i-1, which the MMA warp has consumed
+        ctl->lse2[par ^ 1][r] = na;
+        ctl->dlt[par ^ 1][r] = nd;
+        s.arrive(ctl->vec_sync);
+      }
+    }
+    const bool row_ok = krow < p.sk;
+    const size_t gk = (static_cast<size_t>(bh) * p.sk + krow) * (kHeadDim * 2);
+    uint8_t* dk = static_cast<uint8_t*>(p.out0) + gk;
+    uint8_t* dv = static_cast<uint8_t*>(p.out1) + gk;
+    if (nq == 0) {
+      // keys no query attends (causal, Sk > Sq): zero gradients
+      if (row_ok) {
+        zero_row(dk);
+        zero_row(dv);
+      }
+    } else if (ok && s.wait(ctl->acc_full, 0, kStatusTimeoutSoftmax)) {
+      ptx::tc_fence_after();
+#pragma unroll 2
+      for (int c = 0; c < 8; ++c) {
+        uint32_t acc[16];
+        ptx::tmem_ld_32x32b_x16(kTmemBase + lane_off + kColDK + 16 * c, acc);
+        ptx::tmem_wait_ld();
+        if (row_ok) store_cols16(dk + 32 * c, acc, p.scale);
+        ptx::tmem_ld_32x32b_x16(kTmemBase + lane_off + kColDV + 16 * c, acc);
+        ptx::tmem_wait_ld();
+        if (row_ok) store_cols16(dv + 32 * c, acc, 1.0f);
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_alloc_base, kTmemCols);
+  }
+}
+
+}  // namespace bwd
+}  // namespace attn

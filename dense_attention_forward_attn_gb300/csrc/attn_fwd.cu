@@ -11,6 +11,7 @@
 
 #include "../../include/attn_fwd.h"
 #include "attn_fwd_kernel.cuh"
+#include "attn_bwd_kernel.cuh"
 
 namespace {
 
@@ -20,6 +21,7 @@ struct DeviceInfo {
   int num_sms = 0;
   int smem_optin = 0;
   bool attr_set = false;
+  bool bwd_attr_set = false;
 };
 
 constexpr int kMaxDevices = 64;
@@ -51,6 +53,17 @@ int device_info(int dev, DeviceInfo* out) {
       return ATTN_ERR_CUDA;
     }
     d.attr_set = true;
+  }
+  if (!d.bwd_attr_set) {
+    if (cudaFuncSetAttribute(attn::bwd::attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(attn::bwd::kSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(attn::bwd::attn_bwd_dkdv_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(attn::bwd::kSmemBytes)) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    d.bwd_attr_set = true;
   }
   if (!g_encode) {
     void* fn = nullptr;
@@ -266,3 +279,94 @@ int attn_device_status(unsigned int* word, int clear) {
 }
 
 }  // extern "C"
+
+extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                        float* delta, int B, int H, int Sq, int Sk, int D, float scale, int flags,
+                        void* stream) {
+  if (flags & ~ATTN_FLAGS_ALL) return ATTN_ERR_INVALID_ARG;
+  if (flags & ATTN_FLAG_BSHD) return ATTN_ERR_UNSUPPORTED;
+  int rc = check_shape(B, H, Sq, Sk, D);
+  if (rc != ATTN_OK) return rc;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (scale < 0.f) return ATTN_ERR_UNSUPPORTED;
+  const int64_t bh = static_cast<int64_t>(B) * H;
+  if (bh == 0) return ATTN_OK;
+  if (Sq == 0) {
+    if (Sk == 0) return ATTN_OK;
+    // no queries: every key and value gradient is zero
+    if (!dk || !dv) return ATTN_ERR_INVALID_ARG;
+    const size_t nk = static_cast<size_t>(bh) * Sk * D * 2;
+    if (cudaMemsetAsync(dk, 0, nk, static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+        cudaMemsetAsync(dv, 0, nk, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    return ATTN_OK;
+  }
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !delta)
+    return ATTN_ERR_INVALID_ARG;
+  auto mis16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+  if (mis16(q) || mis16(k) || mis16(v) || mis16(o) || mis16(dout) || mis16(dq) || mis16(dk) ||
+      mis16(dv))
+    return ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(delta) & 3u))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t nq = static_cast<size_t>(bh) * Sq * D * 2, nk = static_cast<size_t>(bh) * Sk * D * 2;
+  const size_t nl = static_cast<size_t>(bh) * Sq * 4;
+  const void* ins[6] = {q, k, v, o, dout, lse};
+  const size_t in_n[6] = {nq, nk, nk, nq, nq, nl};
+  void* outs[4] = {dq, dk, dv, delta};
+  const size_t out_n[4] = {nq, nk, nk, nl};
+  for (int a = 0; a < 4; ++a) {
+    for (int b = 0; b < 6; ++b)
+      if (overlaps(outs[a], out_n[a], ins[b], in_n[b])) return ATTN_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 4; ++b)
+      if (overlaps(outs[a], out_n[a], outs[b], out_n[b])) return ATTN_ERR_INVALID_ARG;
+  }
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  DeviceInfo info;
+  rc = device_info(dev, &info);
+  if (rc != ATTN_OK) return rc;
+
+  alignas(64) CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  if (encode_qkv(&tm_q, q, B, H, Sq, false) != ATTN_OK ||
+      encode_qkv(&tm_k, k, B, H, Sk, false) != ATTN_OK ||
+      encode_qkv(&tm_v, v, B, H, Sk, false) != ATTN_OK ||
+      encode_qkv(&tm_do, dout, B, H, Sq, false) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+
+  attn::bwd::Params p;
+  p.lse = lse;
+  p.delta = delta;
+  p.sq = Sq;
+  p.sk = Sk;
+  p.q_tiles = ceil_div(Sq, attn::kBlockM);
+  p.kv_tiles = ceil_div(Sk, attn::kBlockN);
+  p.q_valid_last = Sq - (p.q_tiles - 1) * attn::kBlockM;
+  p.kv_valid_last = Sk - (p.kv_tiles - 1) * attn::kBlockN;
+  p.bh = static_cast<int>(bh);
+  p.causal = (flags & ATTN_FLAG_CAUSAL) ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  const int64_t rows = bh * Sq;
+  attn::bwd::attn_bwd_delta_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
+      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), delta, rows);
+  p.out0 = dk;
+  p.out1 = dv;
+  attn::bwd::attn_bwd_dkdv_kernel<<<static_cast<unsigned>(bh * p.kv_tiles), attn::bwd::kThreads,
+                                    attn::bwd::kSmemBytes, st>>>(tm_q, tm_k, tm_v, tm_do, p);
+  p.out0 = dq;
+  p.out1 = nullptr;
+  attn::bwd::attn_bwd_dq_kernel<<<static_cast<unsigned>(bh * p.q_tiles), attn::bwd::kThreads,
+                                  attn::bwd::kSmemBytes, st>>>(tm_q, tm_k, tm_v, tm_do, p);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}

@@ -97,6 +97,34 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                 int Sq, int Sk, int D, float scale, int flags, void* stream);
 
+/*
+ * attn_bwd -- enqueue the backward of attn_fwd(_ex) on `stream`: given the
+ * forward's inputs, its output o and natural-log lse, and dout = dL/dO, write
+ *     dv = P^T dout,   dk = scale * dS^T q,   dq = scale * dS k,
+ *     dS = P o (dout v^T - delta),   delta_i = sum_d dout_id o_id,
+ *     P  = exp(scale * q k^T - lse)  (masked entries 0 with ATTN_FLAG_CAUSAL).
+ * The LSE the forward stores is this pass's residual ("Attention for sm90,
+ * Line by Line", the exp2 question: natural-log units, or the gradients are
+ * wrong while the forward is right).
+ *
+ *   q, o, dout, dq   device, BF16, [B, H, Sq, D] contiguous (dq written)
+ *   k, v, dk, dv     device, BF16, [B, H, Sk, D] contiguous (dk, dv written)
+ *   lse              device, fp32, [B, H, Sq], read (attn_fwd's lse)
+ *   delta            device, fp32, [B, H, Sq]: scratch owned by the caller, written
+ *                    with delta_i and read back by the same call
+ *   flags            0 or ATTN_FLAG_CAUSAL (must match the forward); ATTN_FLAG_BSHD
+ *                    gives ATTN_ERR_UNSUPPORTED
+ *
+ * Sizes, scale, alignment (16 bytes for BF16 tensors, 4 for lse and delta),
+ * ownership and error rules as attn_fwd; no output may overlap any input or
+ * another output.  Sq == 0 zero-fills dk and dv.  Deterministic: every
+ * gradient element is written by exactly one thread, no atomics.
+ * Asynchronous: three kernels (delta, dk/dv, dq) are enqueued in order.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, float* delta, int B, int H,
+             int Sq, int Sk, int D, float scale, int flags, void* stream);
+
 /* Static text for a status code (never NULL). */
 const char* attn_status_string(int status);
 
