@@ -22,6 +22,7 @@ ATTN_ERR_INVALID_ARG = -1
 ATTN_ERR_UNSUPPORTED = -2
 ATTN_ERR_ARCH = -3
 ATTN_ERR_CUDA = -4
+ATTN_ERR_TOO_LARGE = -5
 ATTN_FLAG_CAUSAL = 1
 ATTN_FLAG_BSHD = 2
 
@@ -38,8 +39,8 @@ class _Plan(ctypes.Structure):
                 ("smem_bytes", ctypes.c_int), ("tmem_cols", ctypes.c_int)]
 
 
-EXPORTS = ("attn_fwd", "attn_fwd_ex", "attn_bwd", "attn_status_string", "attn_fwd_plan",
-           "attn_fwd_work_item", "attn_fwd_schedule", "attn_device_status")
+EXPORTS = ("attn_fwd", "attn_fwd_ex", "attn_bwd", "attn_bwd_noalloc", "attn_status_string",
+           "attn_fwd_plan", "attn_fwd_work_item", "attn_fwd_schedule", "attn_device_status")
 
 
 def lib_path() -> str:
@@ -55,6 +56,9 @@ def _bind(lib):
     lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32,
                              i32, vp]
     lib.attn_bwd.restype = i32
+    lib.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                     f32, i32, vp]
+    lib.attn_bwd_noalloc.restype = i32
     lib.attn_status_string.argtypes = [i32]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_fwd_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(_Plan)]

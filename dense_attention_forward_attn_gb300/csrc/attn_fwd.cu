@@ -137,6 +137,8 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_UNSUPPORTED: return "unsupported shape or parameter";
     case ATTN_ERR_ARCH: return "device is not a compute capability 10.3 (GB300) GPU";
     case ATTN_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case ATTN_ERR_TOO_LARGE:
+      return "problem exceeds the fixed scratch of the allocation-free entry point";
     default: return "unknown status";
   }
 }
@@ -369,4 +371,49 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
                                   attn::bwd::kSmemBytes, st>>>(tm_q, tm_k, tm_v, tm_do, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
+}
+
+// ------------------------------------------------------------------ allocation-free backward
+// Scratch for attn_bwd_noalloc: the per-query-row delta of the backward lives in this fixed
+// device array instead of a buffer the caller allocates.  Every GPU that loads the library holds
+// it (4 MiB) until the process exits.  Host code must not use its name as a device address: the
+// address is looked up once per device with cudaGetSymbolAddress.
+namespace {
+
+constexpr int64_t kNoAllocDeltaMax = int64_t(1) << 20;   // floats: B * H * Sq <= 1,048,576
+static __device__ __align__(256) float g_noalloc_delta[kNoAllocDeltaMax];
+
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+}  // namespace
+
+extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                                const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                                int B, int H, int Sq, int Sk, int D, float scale, int flags,
+                                void* stream) {
+  if (B < 0 || H < 0 || Sq < 0) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(B) * H * Sq > kNoAllocDeltaMax) return ATTN_ERR_TOO_LARGE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  float* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_noalloc_delta) != cudaSuccess || ptr == nullptr) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+      }
+      g_noalloc_ptr[dev] = static_cast<float*>(ptr);
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  // delta is written in full by the backward's first kernel before it is read, so the array's
+  // leftover contents from an earlier call never matter.
+  return attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, scratch, B, H, Sq, Sk, D, scale, flags,
+                  stream);
 }

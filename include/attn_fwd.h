@@ -36,7 +36,8 @@ typedef enum attn_status {
   ATTN_ERR_INVALID_ARG = -1, /* null/misaligned pointer, negative size, aliasing, bad scale */
   ATTN_ERR_UNSUPPORTED = -2, /* valid request outside what this build supports (D != 128, ...) */
   ATTN_ERR_ARCH = -3,        /* the current device is not a compute capability 10.3 GPU */
-  ATTN_ERR_CUDA = -4         /* a CUDA runtime/driver call failed (launch, tensor-map encode) */
+  ATTN_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed (launch, tensor-map encode) */
+  ATTN_ERR_TOO_LARGE = -5    /* beyond the fixed scratch size of attn_bwd_noalloc */
 } attn_status;
 
 /*
@@ -124,6 +125,33 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
              const float* lse, void* dq, void* dk, void* dv, float* delta, int B, int H,
              int Sq, int Sk, int D, float scale, int flags, void* stream);
+
+/*
+ * attn_bwd_noalloc -- attn_bwd for callers that cannot allocate device memory.
+ * (No counterpart in the pages; this is a property of the library, not of the
+ * method.)  Some callers may not call cudaMalloc around this library: code
+ * running under a memory budget or inside an allocator of its own, embedders
+ * that own every device allocation, or paths where an allocation would
+ * synchronise the device.  attn_bwd needs a [B, H, Sq] fp32 scratch buffer
+ * (delta); this entry point takes no such buffer and uses a fixed array
+ * compiled into the library instead, so it allocates nothing: no cudaMalloc,
+ * cudaFree or allocating library call, on any call.
+ *
+ * Arguments as attn_bwd without `delta`.  Limit: B * H * Sq <= 1,048,576
+ * (the array is 4 MiB); larger problems return ATTN_ERR_TOO_LARGE without
+ * launching.  Every GPU that loads the library holds the 4 MiB array until the
+ * process exits.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  All calls share the one array: two calls whose kernels
+ * overlap on the GPU (different streams, no ordering between them) race on it
+ * and give wrong gradients.  Calls ordered on one stream are safe; the array
+ * keeps the last call's contents, which the next call overwrites before reading.
+ */
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                     const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                     int H, int Sq, int Sk, int D, float scale, int flags, void* stream);
 
 /* Static text for a status code (never NULL). */
 const char* attn_status_string(int status);
