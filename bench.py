@@ -10,6 +10,12 @@ BF16 peak.  Every input set (Q+K+V = 192 MiB per shape) is larger than the
 129 MB L2, so no explicit flush is needed between timed iterations.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--row dense|causal|bshd|backward|backward-causal]
+
+--row (default dense, the headline above) times the same sweep on one of the
+other built rows instead: the causal forward (half of 4*B*H*S^2*D counted),
+the [B,S,H,D] forward, or the backward (dQ, dK, dV; 2.5x the forward FLOPs
+counted, the convention of the FlashAttention papers).
 
 --impl reference times the fp64 CPU oracle (the only reference this path has)
 on bounded samples of the same workload, on the host cores.
@@ -36,6 +42,19 @@ METRIC = "attention fwd TFLOPS (4·B·H·S²·D) at S=4K/8K/16K, % of GB300 BF16
 UNIT = "TFLOP/s"
 WORKLOAD = "S=4K/8K/16K sweep (B=4/2/1, H=16, D=128, BF16, non-causal)"
 FALLBACK_BF16_TFLOPS = 1900.0
+
+# --row: (metric, workload, FLOP factor on 4*B*H*S^2*D)
+ROWS = {
+    "dense": (METRIC, WORKLOAD, 1.0),
+    "causal": ("attention fwd TFLOPS, causal (half of 4·B·H·S²·D counted) at S=4K/8K/16K",
+               "S=4K/8K/16K sweep (B=4/2/1, H=16, D=128, BF16, causal top-left)", 0.5),
+    "bshd": ("attention fwd TFLOPS (4·B·H·S²·D), [B,S,H,D] tensors, at S=4K/8K/16K",
+             "S=4K/8K/16K sweep (B=4/2/1, H=16, D=128, BF16, non-causal, BSHD layout)", 1.0),
+    "backward": ("attention bwd TFLOPS (2.5 × 4·B·H·S²·D) at S=4K/8K/16K",
+                 "S=4K/8K/16K sweep (B=4/2/1, H=16, D=128, BF16, non-causal), dQ/dK/dV", 2.5),
+    "backward-causal": ("attention bwd TFLOPS, causal (1.25 × 4·B·H·S²·D) at S=4K/8K/16K",
+                        "S=4K/8K/16K sweep (B=4/2/1, H=16, D=128, BF16, causal), dQ/dK/dV", 1.25),
+}
 
 
 def _peaks():
@@ -113,9 +132,10 @@ def _dist():
 
 
 def _source_sha() -> str:
+    """Hash of the forward kernel's device source (the files its code is compiled from)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_attention_forward_attn_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in ("attn_fwd_kernel.cuh", "ptx.cuh"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -210,23 +230,53 @@ def run_ours(args):
 
     from dense_attention_forward_attn_gb300 import attn, workloads as wl
 
+    row = args.row
+    metric, workload, flop_factor = ROWS[row]
+    causal = row in ("causal", "backward-causal")
+    layout = "bshd" if row == "bshd" else "bhsd"
+    backward = row.startswith("backward")
     shapes = []
     for w in wl.HEADLINE:
         qb, kb, vb = wl.workload_inputs_bits(w)
-        host = [wl.bits_to_torch(x).pin_memory() for x in (qb, kb, vb)]
+        host = [wl.bits_to_torch(x) for x in (qb, kb, vb)]
+        if layout == "bshd":
+            host = [t.transpose(1, 2).contiguous() for t in host]
+        host = [t.pin_memory() for t in host]
         d = [t.to(dev) for t in host]
         o = torch.empty_like(d[0])
         lse = torch.empty(w.B, w.H, w.Sq, dtype=torch.float32, device=dev)
-        shapes.append((w, (qb, kb, vb), host, d, o, lse))
-    flops = sum(w.flops for w, *_ in shapes)
+        extra = None
+        if backward:
+            # O and LSE of the forward, an upstream gradient dO, and the gradient buffers
+            attn.fwd_into(d[0], d[1], d[2], o, lse, w.scale, causal=causal)
+            dout = wl.bits_to_torch(wl.make_inputs_bits(w.B, w.H, w.Sq, w.Sq, w.D,
+                                                        seed=w.seeds[0] + 100)[0]).to(dev)
+            extra = (dout, torch.empty_like(d[0]), torch.empty_like(d[1]), torch.empty_like(d[2]),
+                     torch.empty(w.B, w.H, w.Sq, dtype=torch.float32, device=dev))
+        shapes.append((w, (qb, kb, vb), host, d, o, lse, extra))
+    flops = flop_factor * sum(w.flops for w, *_ in shapes)
     stream = torch.cuda.current_stream()
     attn.device_status(clear=True)
+    lib = attn.library()
+    bwd_flags = attn.ATTN_FLAG_CAUSAL if causal else 0
+
+    def one(w, d, o, lse, extra):
+        if not backward:
+            attn.fwd_into(d[0], d[1], d[2], o, lse, w.scale, causal=causal, layout=layout)
+            return
+        dout, dq, dk, dv, delta = extra
+        rc = lib.attn_bwd(d[0].data_ptr(), d[1].data_ptr(), d[2].data_ptr(), o.data_ptr(),
+                          dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                          dv.data_ptr(), delta.data_ptr(), w.B, w.H, w.Sq, w.Sk, w.D, w.scale,
+                          bwd_flags, stream.cuda_stream)
+        if rc != attn.ATTN_OK:
+            raise attn.AttnError(rc, "attn_bwd")
 
     def step(evs=None):
-        for i, (w, _, _, d, o, lse) in enumerate(shapes):
+        for i, (w, _, _, d, o, lse, extra) in enumerate(shapes):
             if evs is not None:
                 evs[i][0].record(stream)
-            attn.fwd_into(d[0], d[1], d[2], o, lse, w.scale)
+            one(w, d, o, lse, extra)
             if evs is not None:
                 evs[i][1].record(stream)
 
@@ -266,23 +316,28 @@ def run_ours(args):
         avg = sum(ms) / len(ms)
         kernel_ms_total += avg
         per_cfg[w.name] = {"ms_avg": round(avg, 4), "ms_min": round(min(ms), 4),
-                           "tflops": round(w.flops / (avg * 1e-3) / 1e12, 1)}
+                           "tflops": round(flop_factor * w.flops / (avg * 1e-3) / 1e12, 1)}
     status = attn.device_status()
 
-    # ---------------- end to end through the public API with host buffers
-    h2d = sum(sum(t.numel() * t.element_size() for t in host) for _, _, host, *_ in shapes)
-    d2h = sum(o.numel() * o.element_size() + lse.numel() * 4 for *_, o, lse in shapes)
-    e2e_steps = max(2, min(args.steps, 10))
-    for w, _, host, *_ in shapes:   # warm the pinned output buffers
-        attn.fwd(host[0], host[1], host[2], scale=w.scale)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        for w, _, host, *_ in shapes:
-            o_h, lse_h = attn.fwd(host[0], host[1], host[2], scale=w.scale)
-    torch.cuda.synchronize()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
-    e2e_val = ws * flops / (e2e_ms * 1e-3) / 1e12
+    # ---------------- end to end through the public API with host buffers (forward rows)
+    e2e = None
+    if not backward:
+        h2d = sum(sum(t.numel() * t.element_size() for t in host) for _, _, host, *_ in shapes)
+        d2h = sum(o.numel() * o.element_size() + lse.numel() * 4 for *_, o, lse, _x in shapes)
+        e2e_steps = max(2, min(args.steps, 10))
+        for w, _, host, *_ in shapes:   # warm the pinned output buffers
+            attn.fwd(host[0], host[1], host[2], scale=w.scale, causal=causal, layout=layout)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            for w, _, host, *_ in shapes:
+                o_h, lse_h = attn.fwd(host[0], host[1], host[2], scale=w.scale, causal=causal,
+                                      layout=layout)
+        torch.cuda.synchronize()
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
+        e2e = {"value": round(ws * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e2e_ms, 3)}
 
     if rank != 0:
         if ws > 1:
@@ -293,19 +348,19 @@ def run_ours(args):
     achieved = flops / (kernel_ms_total * 1e-3) / 1e12
     traffic = None
     tr = [_traffic_for(w.name) for w, *_ in shapes]
-    if all(t is not None for t in tr):
+    if row == "dense" and all(t is not None for t in tr):
         traffic = sum(tr) / len(tr)
     cpu = None
-    if ws == 1 and not args.no_cpu_baseline:
+    if ws == 1 and not args.no_cpu_baseline and row == "dense":
         v, cores, sample, _t = oracle_sample_tflops([(w, bits) for w, bits, *_ in shapes], 12.0)
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{sample} (fp64 oracle, random query rows, ~12 s total)"}
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
+        "metric": metric, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "shapes": [w.describe() for w, *_ in shapes],
+        "config": {"workload": workload, "shapes": [w.describe() for w, *_ in shapes],
                    "per_shape": per_cfg, "l2": "inputs larger than L2 (Q+K+V = 192 MiB per shape)",
                    "parallelism": "replicas" if ws > 1 else "single GPU",
                    "frac_of_peak": round(value / peak, 4), "device_status": status},
@@ -313,9 +368,8 @@ def run_ours(args):
                      "unit": UNIT, "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_kind": f"{peak_kind} burst bf16 (cuBLAS)"},
         "cpu_baseline": cpu,
-        "e2e": {"value": round(e2e_val, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
-        "gpu_launches": args.steps * len(shapes),
+        "e2e": e2e,
+        "gpu_launches": args.steps * len(shapes) * (3 if backward else 1),
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)
@@ -331,7 +385,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--row", choices=sorted(ROWS), default="dense",
+                    help="which built row to time (default: the dense headline)")
     args = ap.parse_args()
+    if args.impl == "reference" and args.row != "dense":
+        ap.error("--impl reference times the dense headline only")
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
