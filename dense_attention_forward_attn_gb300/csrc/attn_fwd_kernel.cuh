@@ -478,22 +478,23 @@ __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
 
 // ------------------------------------------------------------------ softmax warpgroups
 // Raw scores of columns >= valid become -inf (they then never hold the row max).
-__device__ __forceinline__ void mask_scores(uint32_t (&sr)[4][32], int valid) {
+// Masked columns (>= valid) get the raw score -inf: they never set the row max, and their P is
+// exp2(-inf) = 0 (the multiplier is always positive, so -inf stays -inf).  keep = 0 (zero scale)
+// also turns every kept score into 0, so each of them gets P = exp2(0) = 1.
+__device__ __forceinline__ void mask_scores(uint32_t (&sr)[4][32], int valid, uint32_t keep) {
 #pragma unroll
   for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
     for (int i = 0; i < 32; ++i)
-      if (cc * 32 + i >= valid) sr[cc][i] = 0xff800000u;
+      sr[cc][i] = cc * 32 + i >= valid ? 0xff800000u : (sr[cc][i] & keep);
 }
 
 // P of one KV tile: exp2(s * scale_log2 - m_kept), two columns per packed FMA, packed BF16 into
 // TMEM over the upper half of this stage's S columns; the upper 96 columns are published first
-// (p_hi_full: P*V K-steps 2..7 may start), then the lower 32 (p_lo_full).  With MASK, columns
-// >= valid get P = 0 (also when scale is 0).  Returns the row sum of the tile's fp32 P.
-template <bool MASK>
+// (p_hi_full: P*V K-steps 2..7 may start), then the lower 32 (p_lo_full).  Masked columns arrive
+// as -inf and come out as 0.  Returns the row sum of the tile's fp32 P.
 __device__ __forceinline__ float produce_p(const Ctx& c, int q, const uint32_t (&sr)[4][32],
-                                           float scale_log2, float m_kept, int valid,
-                                           uint32_t taddr_s) {
+                                           float scale_log2, float m_kept, uint32_t taddr_s) {
   SmemCtl* ctl = c.ctl;
   const float2 c2 = make_float2(scale_log2, scale_log2);
   const float2 nm2 = make_float2(-m_kept, -m_kept);
@@ -508,11 +509,6 @@ __device__ __forceinline__ float produce_p(const Ctx& c, int q, const uint32_t (
                             c2, nm2);
       x.x = ptx::ex2_ftz(x.x);
       x.y = ptx::ex2_ftz(x.y);
-      if (MASK) {
-        const int col = cc * 32 + 2 * i;
-        x.x = col < valid ? x.x : 0.f;
-        x.y = col + 1 < valid ? x.y : 0.f;
-      }
       if (i & 1) acc1 = ptx::fadd2(acc1, x); else acc0 = ptx::fadd2(acc0, x);
       pk[i] = ptx::pack_bf16x2(x.x, x.y);
     }
@@ -553,7 +549,11 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
   const uint32_t row_base = 32u * (c.warp & 3u);
   const int row = static_cast<int>(row_base + c.lane);
   const uint32_t taddr_s = c.tmem + (row_base << 16) + col_s(q);
-  const float scale_log2 = p.scale_log2;
+  // A zero scale makes every kept score 0 (mask_scores on every tile) and uses multiplier 1, so
+  // masked columns still give -inf * 1 = -inf rather than -inf * 0 = NaN.
+  const bool zero_scale = p.scale_log2 == 0.f;
+  const float scale_log2 = zero_scale ? 1.f : p.scale_log2;
+  const uint32_t keep = zero_scale ? 0u : 0xffffffffu;
   uint32_t tphase = 0;
   uint32_t items_q = 0;
 
@@ -577,11 +577,11 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
       // 128 (zero-filled key rows), and, with the causal mask, past this row on the diagonal
       // tile.  They must not enter the max and get P = 0 below.  The test is warp-uniform.
       const bool diag = p.causal != 0 && j == qtile;
-      const bool partial = diag || (j == p.kv_tiles - 1 && p.kv_valid_last < kBlockN);
+      const bool partial = zero_scale || diag || (j == p.kv_tiles - 1 && p.kv_valid_last < kBlockN);
       int valid = kBlockN;
       if (j == p.kv_tiles - 1) valid = p.kv_valid_last;
       if (diag) valid = min(valid, row + 1);
-      if (partial) mask_scores(sr, valid);
+      if (partial) mask_scores(sr, valid, keep);
 
       // Row max over the raw scores: a 3-input-max tree (depth 5, 65 instructions).
       const float m_tile = row_max_128(sr) * scale_log2;
@@ -596,8 +596,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
       ctl->alpha[q][tphase][row] = alpha;
       c.arrive(ctl->stats_full[q]);
 
-      l += partial ? produce_p<true>(c, q, sr, scale_log2, m_kept, valid, taddr_s)
-                   : produce_p<false>(c, q, sr, scale_log2, m_kept, kBlockN, taddr_s);
+      l += produce_p(c, q, sr, scale_log2, m_kept, taddr_s);
       tphase ^= 1u;
     }
     ctl->row_m[q][items_q & 1u][row] = m_kept;
