@@ -270,8 +270,10 @@ def test_causal_full_size_sampled_rows(name):
 
 @pytest.mark.parametrize("shape,causal", [
     ((2, 3, 256, 384), False),
-    ((1, 4, 300, 300), True),
+    ((3, 2, 512, 512), True),
+    ((1, 4, 300, 300), True),     # ragged: rows past S of each batch read as zeros
     ((2, 2, 129, 1000), False),
+    ((2, 2, 256, 200), False),
 ])
 def test_bshd_layout(shape, causal):
     B, H, Sq, Sk = shape
@@ -288,3 +290,19 @@ def test_bshd_layout(shape, causal):
     # bitwise equal to the [B,H,S,D] path on the same values
     o2, lse2 = attn.fwd(*(wl.bits_to_torch(x).cuda() for x in (qb, kb, vb)), scale=scale, causal=causal)
     assert torch.equal(o2, o.transpose(1, 2).contiguous()) and torch.equal(lse2, lse)
+
+
+def test_bshd_full_size_sampled_rows():
+    """S=4K (B=4, H=16) in [B,S,H,D]: sampled rows against the oracle, bitwise equal to BHSD."""
+    w = wl.S4K
+    qb, kb, vb = wl.workload_inputs_bits(w)
+    q, k, v = (wl.bits_to_torch(np.ascontiguousarray(x.transpose(0, 2, 1, 3))).cuda() for x in (qb, kb, vb))
+    o, lse = attn.fwd(q, k, v, scale=w.scale, layout="bshd")
+    o2, lse2 = attn.fwd(*(wl.bits_to_torch(x).cuda() for x in (qb, kb, vb)), scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, o.transpose(1, 2).contiguous()) and torch.equal(lse2, lse)
+    bh, rows = _rows_sample(w, 200, seed=5)
+    o_ref, lse_ref = oracle.attn_fwd_rows(qb, kb, vb, w.scale, bh, rows)
+    o_bhsd = o2.float().cpu().numpy().astype(np.float64).reshape(-1, w.Sq, w.D)
+    _assert_close(o_bhsd[bh, rows], o_ref, lse.cpu().numpy().astype(np.float64).reshape(-1, w.Sq)[bh, rows],
+                  lse_ref)
