@@ -107,7 +107,9 @@ struct alignas(8) SmemCtl {
   uint64_t p_lo_full[2];   // softmax (P cols 0..31) -> MMA
   uint64_t stats_full[2];  // softmax -> correction: per-row rescale factor published
   uint64_t o_full[2];      // MMA -> correction: last P*V of the item done
-  uint64_t final_full[2];  // softmax -> correction: final row max / row sum published
+  // softmax -> correction: final row max / row sum of an item published, one barrier per item
+  // parity: the softmax may publish item r+1 before the correction has read item r.
+  uint64_t final_full[2][2];   // [stage][item parity]
   uint64_t drain;
   uint32_t tmem_base;
   volatile int abort_flag;
@@ -601,7 +603,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
     }
     ctl->row_m[q][items_q & 1u][row] = m_kept;
     ctl->row_l[q][items_q & 1u][row] = l;
-    c.arrive(ctl->final_full[q]);
+    c.arrive(ctl->final_full[q][items_q & 1u]);
     ++items_q;
   }
 }
@@ -610,7 +612,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
 __device__ __forceinline__ bool epilogue(const Ctx& c, const Params& p, int q, const WorkItem& w,
                                          uint32_t idx) {
   SmemCtl* ctl = c.ctl;
-  if (!c.wait(ctl->final_full[q], idx & 1u, kStatusTimeoutCorrection)) return false;
+  if (!c.wait(ctl->final_full[q][idx & 1u], (idx >> 1) & 1u, kStatusTimeoutCorrection)) return false;
   if (!c.wait(ctl->o_full[q], idx & 1u, kStatusTimeoutCorrection)) return false;
   ptx::tc_fence_after();
   const uint32_t row_base = 32u * (c.warp & 3u);
@@ -723,7 +725,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ptx::mbar_init(c.bar(ctl->p_lo_full[q]), kArrivePerWG);
       ptx::mbar_init(c.bar(ctl->stats_full[q]), kArrivePerWG);
       ptx::mbar_init(c.bar(ctl->o_full[q]), 1);
-      ptx::mbar_init(c.bar(ctl->final_full[q]), kArrivePerWG);
+      ptx::mbar_init(c.bar(ctl->final_full[q][0]), kArrivePerWG);
+      ptx::mbar_init(c.bar(ctl->final_full[q][1]), kArrivePerWG);
     }
     for (int s = 0; s < kKvStages; ++s) {
       ptx::mbar_init(c.bar(ctl->kv_full[s]), 1);

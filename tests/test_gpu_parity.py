@@ -119,6 +119,28 @@ def test_persistent_loop_over_many_items():
     _assert_close(o.reshape(B * H, Sq, 128)[bh, rows], o_ref, lse.reshape(B * H, Sq)[bh, rows], lse_ref)
 
 
+@pytest.mark.parametrize("shape,causal", [
+    ((1, 400, 256, 128), False),   # one KV tile per item: a softmax finishes an item per tile
+    ((2, 170, 200, 60), False),
+    ((1, 330, 256, 256), True),    # causal pairs whose first Q tile attends a single KV tile
+])
+def test_many_short_items_per_cta(shape, causal):
+    """Items of one or two KV tiles, several per CTA: the softmax of a stage can publish an item's
+    final row statistics before the epilogue has read those of the item before it."""
+    B, H, Sq, Sk = shape
+    qb, kb, vb = wl.make_inputs_bits(B, H, Sq, Sk, 128, seed=31)
+    scale = 1.0 / math.sqrt(128)
+    o, lse = _run(qb, kb, vb, scale, causal=causal)
+    o2, lse2 = _run(qb, kb, vb, scale, causal=causal)
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+    rng = np.random.Generator(np.random.PCG64(7))
+    bh = rng.integers(0, B * H, 1500)
+    rows = rng.integers(0, Sq, 1500)
+    o_ref, lse_ref = oracle.attn_fwd_rows(qb, kb, vb, scale, bh, rows, causal=causal)
+    _assert_close(o.reshape(B * H, Sq, 128)[bh, rows], o_ref, lse.reshape(B * H, Sq)[bh, rows], lse_ref)
+    assert attn.device_status() == 0
+
+
 def test_zero_scale_is_uniform_average():
     qb, kb, vb = wl.make_inputs_bits(1, 2, 256, 384, 128, seed=3)
     o, lse = _run(qb, kb, vb, 0.0)
