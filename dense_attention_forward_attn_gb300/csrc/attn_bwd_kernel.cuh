@@ -52,6 +52,9 @@ struct alignas(8) SmemCtl {
   uint64_t mma_full;            // MMA -> elementwise: the two score-like tiles are in TMEM
   uint64_t ew_full;             // elementwise -> MMA: BF16 operands written into TMEM
   uint64_t acc_full;            // MMA -> elementwise: the accumulators are final
+  // dK/dV kernel, per Q tile: S^T and dP^T in TMEM (MMA -> elementwise), P^T and dS^T written
+  // back (elementwise -> MMA).  Separate barriers let dV += P^T dO start before dS^T exists.
+  uint64_t s_full, dp_full, p_ready, ds_ready;
   uint64_t vec_sync;            // elementwise warps exchanged per-column vectors (dK/dV)
   uint64_t drain;
   uint32_t tmem_base;
@@ -192,6 +195,10 @@ __device__ __forceinline__ void init_barriers(SmemCtl* ctl, const Sync& s) {
   ptx::mbar_init(s.bar(ctl->mma_full), 1);
   ptx::mbar_init(s.bar(ctl->ew_full), 4);
   ptx::mbar_init(s.bar(ctl->acc_full), 1);
+  ptx::mbar_init(s.bar(ctl->s_full), 1);
+  ptx::mbar_init(s.bar(ctl->dp_full), 1);
+  ptx::mbar_init(s.bar(ctl->p_ready), 4);
+  ptx::mbar_init(s.bar(ctl->ds_ready), 4);
   ptx::mbar_init(s.bar(ctl->vec_sync), 4);
   ptx::mbar_init(s.bar(ctl->drain), 1);
   ctl->abort_flag = 0;
@@ -417,34 +424,69 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     // resident: K, V of this tile; streamed: Q_i, dO_i
     stream_tiles(L, s, &tm_k, &tm_v, kt * kBlockN, &tm_q, &tm_do, q0, nq, bh);
   } else if (tmem_ok && warp == kMmaWarp && nq > 0) {
+    // Per Q tile i the tensor pipe runs dV(i), S(i+1), dK(i), dP(i+1): S^T(i+1) overwrites
+    // P^T(i) only after dV(i) has been issued, dP^T(i+1) overwrites dS^T(i) only after dK(i),
+    // and the elementwise work on tile i+1 overlaps the products of tile i.
     const bool leader = ptx::elect_one();
     bool ok = s.wait(ctl->fixed_full, 0, kStatusTimeoutMma);
     int slot = 0;
     uint32_t phase = 0;
-    for (int i = 0; ok && i < nq; ++i) {
-      const int qs = slot;
-      if (!(ok = s.wait(ctl->ring_full[qs], phase, kStatusTimeoutMma))) break;
+    auto next_slot = [&](int& out) -> bool {
+      out = slot;
+      const bool r = s.wait(ctl->ring_full[slot], phase, kStatusTimeoutMma);
       if (++slot == kRing) { slot = 0; phase ^= 1u; }
-      const int ds = slot;
-      if (!(ok = s.wait(ctl->ring_full[ds], phase, kStatusTimeoutMma))) break;
-      if (++slot == kRing) { slot = 0; phase ^= 1u; }
+      return r;
+    };
+    int qs = 0, ds = 0;
+    ok = ok && next_slot(qs) && next_slot(ds);
+    if (ok) {
       ptx::tc_fence_after();
       if (leader) {
         mma_kmajor(kTmemBase + kColST, L.fixed(0), L.ring(qs));    // S^T = K Q^T
+        ptx::mma_commit(s.bar(ctl->s_full));
         mma_kmajor(kTmemBase + kColDPT, L.fixed(1), L.ring(ds));   // dP^T = V dO^T
-        ptx::mma_commit(s.bar(ctl->mma_full));
+        ptx::mma_commit(s.bar(ctl->dp_full));
       }
       __syncwarp();
-      if (!(ok = s.wait(ctl->ew_full, i & 1u, kStatusTimeoutMma))) break;
+    }
+    for (int i = 0; ok && i < nq; ++i) {
+      const bool more = i + 1 < nq;
+      if (!(ok = s.wait(ctl->p_ready, i & 1u, kStatusTimeoutMma))) break;
       ptx::tc_fence_after();
       if (leader) {
         mma_tmem_a(kTmemBase + kColDV, kTmemBase + kColST + kColP, L.ring(ds), i > 0);   // dV += P^T dO
-        mma_tmem_a(kTmemBase + kColDK, kTmemBase + kColDPT + kColP, L.ring(qs), i > 0);  // dK += dS^T Q
-        ptx::mma_commit(s.bar(ctl->ring_empty[qs]));
         ptx::mma_commit(s.bar(ctl->ring_empty[ds]));
-        if (i == nq - 1) ptx::mma_commit(s.bar(ctl->acc_full));
       }
       __syncwarp();
+      int qn = 0, dn = 0;
+      if (more) {
+        if (!(ok = next_slot(qn))) break;
+        ptx::tc_fence_after();
+        if (leader) {
+          mma_kmajor(kTmemBase + kColST, L.fixed(0), L.ring(qn));
+          ptx::mma_commit(s.bar(ctl->s_full));
+        }
+        __syncwarp();
+      }
+      if (!(ok = s.wait(ctl->ds_ready, i & 1u, kStatusTimeoutMma))) break;
+      ptx::tc_fence_after();
+      if (leader) {
+        mma_tmem_a(kTmemBase + kColDK, kTmemBase + kColDPT + kColP, L.ring(qs), i > 0);  // dK += dS^T Q
+        ptx::mma_commit(s.bar(ctl->ring_empty[qs]));
+        if (!more) ptx::mma_commit(s.bar(ctl->acc_full));
+      }
+      __syncwarp();
+      if (more) {
+        if (!(ok = next_slot(dn))) break;
+        ptx::tc_fence_after();
+        if (leader) {
+          mma_kmajor(kTmemBase + kColDPT, L.fixed(1), L.ring(dn));
+          ptx::mma_commit(s.bar(ctl->dp_full));
+        }
+        __syncwarp();
+      }
+      qs = qn;
+      ds = dn;
     }
     if (leader) ptx::mma_commit(s.bar(ctl->drain));
     __syncwarp();
@@ -475,41 +517,61 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       const int par = i & 1;
       if (i + 1 < nq) fetch(i + 1, na, nd);   // next tile's vectors, in flight meanwhile
       if (!(ok = s.wait(ctl->vec_sync, par, kStatusTimeoutSoftmax))) break;
-      if (!(ok = s.wait(ctl->mma_full, par, kStatusTimeoutSoftmax))) break;
+      if (!(ok = s.wait(ctl->s_full, par, kStatusTimeoutSoftmax))) break;
       ptx::tc_fence_after();
       const bool diag = p.causal && q0 + i == kt;   // query column c < key row r is masked
       const float* va = ctl->lse2[par];
       const float* vd = ctl->dlt[par];
+      // P^T = exp2(S^T * scale_log2 - LSE_col * log2 e), kept in fp32 for dS^T; high chunk
+      // first, since the packed P^T of chunk c lands on S^T columns 64+16c.., already read.
+      float pf[4][32];
 #pragma unroll
       for (int c = 3; c >= 0; --c) {
-        uint32_t sr[32], dr[32];
+        uint32_t sr[32];
         ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColST + 32 * c, sr);
-        ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColDPT + 32 * c, dr);
         ptx::tmem_wait_ld();
-        uint32_t pp[16], pd[16];
+        uint32_t pp[16];
 #pragma unroll
         for (int i2 = 0; i2 < 16; ++i2) {
           const int col = 32 * c + 2 * i2;
           const float2 a = *reinterpret_cast<const float2*>(va + col);
-          const float2 d = *reinterpret_cast<const float2*>(vd + col);
           float p0 = ptx::ex2_ftz(fmaf(__uint_as_float(sr[2 * i2]), p.scale_log2, -a.x));
           float p1 = ptx::ex2_ftz(fmaf(__uint_as_float(sr[2 * i2 + 1]), p.scale_log2, -a.y));
           if (diag) {
             p0 = col < r ? 0.f : p0;
             p1 = col + 1 < r ? 0.f : p1;
           }
+          pf[c][2 * i2] = p0;
+          pf[c][2 * i2 + 1] = p1;
           pp[i2] = ptx::pack_bf16x2(p0, p1);
-          pd[i2] = ptx::pack_bf16x2(p0 * (__uint_as_float(dr[2 * i2]) - d.x),
-                                    p1 * (__uint_as_float(dr[2 * i2 + 1]) - d.y));
         }
         ptx::tmem_st_32x32b_x16(kTmemBase + lane_off + kColST + kColP + 16 * c, pp);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      s.arrive(ctl->p_ready);
+      // dS^T = P^T o (dP^T - delta_col), packed over the upper half of dP^T the same way.
+      if (!(ok = s.wait(ctl->dp_full, par, kStatusTimeoutSoftmax))) break;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int c = 3; c >= 0; --c) {
+        uint32_t dr[32];
+        ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColDPT + 32 * c, dr);
+        ptx::tmem_wait_ld();
+        uint32_t pd[16];
+#pragma unroll
+        for (int i2 = 0; i2 < 16; ++i2) {
+          const float2 d = *reinterpret_cast<const float2*>(vd + 32 * c + 2 * i2);
+          pd[i2] = ptx::pack_bf16x2(pf[c][2 * i2] * (__uint_as_float(dr[2 * i2]) - d.x),
+                                    pf[c][2 * i2 + 1] * (__uint_as_float(dr[2 * i2 + 1]) - d.y));
+        }
         ptx::tmem_st_32x32b_x16(kTmemBase + lane_off + kColDPT + kColP + 16 * c, pd);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      s.arrive(ctl->ew_full);
+      s.arrive(ctl->ds_ready);
       if (i + 1 < nq) {
-        // the other buffer was last read at tile i-1, which the MMA warp has consumed
+        // the other buffer was last read at tile i-1, whose dS^T the MMA warp has consumed
         ctl->lse2[par ^ 1][r] = na;
         ctl->dlt[par ^ 1][r] = nd;
         s.arrive(ctl->vec_sync);
