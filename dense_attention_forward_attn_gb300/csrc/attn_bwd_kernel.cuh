@@ -30,7 +30,12 @@ namespace bwd {
 constexpr int kThreads = 192;
 constexpr int kLoadWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kRing = 4;   // K/V (dQ kernel) or Q/dO (dK/dV kernel) tiles in flight
+// Streamed tiles in flight.  dK/dV kernel: one ring of 4 slots (Q_i, dO_i alternate).  dQ kernel:
+// a K ring of 3 slots (ring slots 0..2: K_j lives from S_j to dQ += dS_j K_j) and a V ring of 2
+// (slots 3..4: V_j only feeds dP_j), so each tile is prefetched two products ahead.
+constexpr int kRing = 5;
+constexpr int kDkdvRing = 4;
+constexpr int kDqKRing = 3, kDqVRing = 2;
 
 struct Params {
   const void* lse;     // fp32 [B,H,Sq], natural log (the forward's output)
@@ -55,6 +60,9 @@ struct alignas(8) SmemCtl {
   // dK/dV kernel, per Q tile: S^T and dP^T in TMEM (MMA -> elementwise), P^T and dS^T written
   // back (elementwise -> MMA).  Separate barriers let dV += P^T dO start before dS^T exists.
   uint64_t s_full, dp_full, p_ready, ds_ready;
+  // dQ kernel: S of KV tile j in TMEM buffer j&1, one barrier per buffer (the product for tile j+2
+  // may complete before the elementwise warps waited for tile j+1).
+  uint64_t sb_full[2];
   uint64_t vec_sync;            // elementwise warps exchanged per-column vectors (dK/dV)
   uint64_t drain;
   uint32_t tmem_base;
@@ -63,8 +71,16 @@ struct alignas(8) SmemCtl {
   float dlt[2][kBlockM];        // dK/dV kernel: delta of the current Q tile's columns
 };
 
-constexpr uint32_t kCtlOffset = (2 + kRing) * kTileBytes;
-constexpr uint32_t kSmemBytes = kCtlOffset + sizeof(SmemCtl) + 1024;
+// dK/dV kernel: 2 resident + 4 ring tiles, control block, 1 KiB to align the base by hand.
+constexpr uint32_t kCtlOffsetDkdv = (2 + kDkdvRing) * kTileBytes;
+constexpr uint32_t kSmemBytesDkdv = kCtlOffsetDkdv + sizeof(SmemCtl) + 1024;
+// dQ kernel: 2 resident + 5 ring tiles and the control block fill the 227 KiB a CTA may have, with
+// no room to realign: the kernel requires the dynamic shared memory to start 1024-aligned (it
+// does when the kernel declares no static shared memory) and checks it.
+constexpr uint32_t kCtlOffsetDq = (2 + kRing) * kTileBytes;
+constexpr uint32_t kSmemBytesDq = kCtlOffsetDq + sizeof(SmemCtl);
+constexpr unsigned kStatusSmemAlign = 1u << 6;   // dynamic shared memory not 1024-aligned
+static_assert(kSmemBytesDq <= 227 * 1024, "dQ kernel shared memory exceeds a CTA's 227 KiB");
 
 // Bounded waits, as in the forward kernel: all 32 lanes call; false = timed out or aborted.
 struct Sync {
@@ -178,11 +194,11 @@ struct Layout {
   __device__ uint32_t ring(int s) const { return base + (2 + s) * kTileBytes; }
 };
 
-__device__ __forceinline__ Layout setup(uint8_t* smem_raw) {
+__device__ __forceinline__ Layout setup(uint8_t* smem_raw, uint32_t ctl_offset) {
   const uint32_t raw = ptx::smem_u32(smem_raw);
   Layout L;
   L.base = (raw + 1023u) & ~1023u;
-  L.ctl = reinterpret_cast<SmemCtl*>(smem_raw + (L.base - raw) + kCtlOffset);
+  L.ctl = reinterpret_cast<SmemCtl*>(smem_raw + (L.base - raw) + ctl_offset);
   return L;
 }
 
@@ -199,6 +215,8 @@ __device__ __forceinline__ void init_barriers(SmemCtl* ctl, const Sync& s) {
   ptx::mbar_init(s.bar(ctl->dp_full), 1);
   ptx::mbar_init(s.bar(ctl->p_ready), 4);
   ptx::mbar_init(s.bar(ctl->ds_ready), 4);
+  ptx::mbar_init(s.bar(ctl->sb_full[0]), 1);
+  ptx::mbar_init(s.bar(ctl->sb_full[1]), 1);
   ptx::mbar_init(s.bar(ctl->vec_sync), 4);
   ptx::mbar_init(s.bar(ctl->drain), 1);
   ctl->abort_flag = 0;
@@ -231,18 +249,20 @@ __device__ __forceinline__ void stream_tiles(const Layout& L, const Sync& s, con
     __syncwarp();
     used |= 1u << slot;
     last_par = (last_par & ~(1u << slot)) | (phase << slot);
-    if (++slot == kRing) { slot = 0; phase ^= 1u; }
+    if (++slot == kDkdvRing) { slot = 0; phase ^= 1u; }
   }
   if (!ok) {
-    for (int i = 0; i < kRing; ++i)
+    for (int i = 0; i < kDkdvRing; ++i)
       if ((used >> i) & 1u) s.drain_wait(ctl->ring_full[i], (last_par >> i) & 1u);
   }
   s.drain_wait(ctl->fixed_full, 0);
 }
 
 // ------------------------------------------------------------------ dQ kernel
-// TMEM: S [0,128) with packed BF16 dS over columns 64..127, dP [128,256), dQ [256,384).
-constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+// TMEM: S double-buffered at [0,128) and [384,512) (KV tile j in buffer j&1, packed BF16 dS over
+// the upper 64 columns of its buffer), dP [128,256), dQ [256,384).
+constexpr uint32_t kColDP = 128, kColDQ = 256;
+__device__ __forceinline__ uint32_t col_sbuf(int j) { return (j & 1) ? 384u : 0u; }
 
 __device__ __forceinline__ void dq_item(const Params& p, int& bh, int& qt, int& nkv) {
   if (p.causal) {   // heaviest Q tiles first
@@ -256,12 +276,56 @@ __device__ __forceinline__ void dq_item(const Params& p, int& bh, int& qt, int& 
   }
 }
 
+// TMA warp of the dQ kernel: Q and dO resident, then K_j into the K ring and V_j into the V ring.
+__device__ __forceinline__ void dq_loads(const Layout& L, const Sync& s, const CUtensorMap* tm_q,
+                                         const CUtensorMap* tm_do, const CUtensorMap* tm_k,
+                                         const CUtensorMap* tm_v, int qrow, int nkv, int bh) {
+  SmemCtl* ctl = L.ctl;
+  if (s.lane == 0) {
+    const uint32_t fb = s.bar(ctl->fixed_full);
+    ptx::mbar_arrive_expect_tx(fb, 2 * kTileBytes);
+    load_tile(L.fixed(0), tm_q, fb, qrow, bh);
+    load_tile(L.fixed(1), tm_do, fb, qrow, bh);
+  }
+  __syncwarp();
+  int ks = 0, vs = 0;
+  uint32_t kph = 0, vph = 0, used = 0, last_par = 0;
+  bool ok = true;
+  auto load = [&](int slot, uint32_t ph, const CUtensorMap* tm, int row) -> bool {
+    if (!s.wait(ctl->ring_empty[slot], ph ^ 1u, kStatusTimeoutLoad)) return false;
+    if (s.lane == 0) {
+      const uint32_t fb = s.bar(ctl->ring_full[slot]);
+      ptx::mbar_arrive_expect_tx(fb, kTileBytes);
+      load_tile(L.ring(slot), tm, fb, row, bh);
+    }
+    __syncwarp();
+    used |= 1u << slot;
+    last_par = (last_par & ~(1u << slot)) | (ph << slot);
+    return true;
+  };
+  for (int j = 0; ok && j < nkv; ++j) {
+    if (!(ok = load(ks, kph, tm_k, j * kBlockN))) break;
+    if (++ks == kDqKRing) { ks = 0; kph ^= 1u; }
+    if (!(ok = load(kDqKRing + vs, vph, tm_v, j * kBlockN))) break;
+    if (++vs == kDqVRing) { vs = 0; vph ^= 1u; }
+  }
+  if (!ok) {
+    for (int i = 0; i < kRing; ++i)
+      if ((used >> i) & 1u) s.drain_wait(ctl->ring_full[i], (last_par >> i) & 1u);
+  }
+  s.drain_wait(ctl->fixed_full, 0);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  const Layout L = setup(smem_raw);
+  if ((ptx::smem_u32(smem_raw) & 1023u) != 0) {   // no room for realignment: skip the CTA
+    if (threadIdx.x == 0) atomicOr(&g_attn_status, kStatusSmemAlign);
+    return;
+  }
+  const Layout L = setup(smem_raw, kCtlOffsetDq);
   SmemCtl* ctl = L.ctl;
   const uint32_t warp = threadIdx.x >> 5;
   Sync s{ctl, threadIdx.x & 31u};
@@ -281,36 +345,69 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   if (!tmem_ok && threadIdx.x == 0) atomicOr(&g_attn_status, kStatusTmemBase);
 
   if (tmem_ok && warp == kLoadWarp) {
-    // resident: Q, dO of this tile; streamed: K_j, V_j
-    stream_tiles(L, s, &tm_q, &tm_do, qt * kBlockM, &tm_k, &tm_v, 0, nkv, bh);
+    dq_loads(L, s, &tm_q, &tm_do, &tm_k, &tm_v, qt * kBlockM, nkv, bh);
   } else if (tmem_ok && warp == kMmaWarp) {
+    // Per KV tile j the tensor pipe runs S(j+1) (into the other S buffer), dQ(j), dP(j+1): the
+    // elementwise work on tile j overlaps S(j+1), and dP(j+1) overwrites dP(j) only after the
+    // elementwise warps have read it (ds_ready).
     const bool leader = ptx::elect_one();
     bool ok = s.wait(ctl->fixed_full, 0, kStatusTimeoutMma);
-    int slot = 0;
-    uint32_t phase = 0;
+    int ks = 0, vs = 0;
+    uint32_t kph = 0, vph = 0;
+    auto next_k = [&](int& out) -> bool {
+      out = ks;
+      const bool r = s.wait(ctl->ring_full[ks], kph, kStatusTimeoutMma);
+      if (++ks == kDqKRing) { ks = 0; kph ^= 1u; }
+      return r;
+    };
+    auto next_v = [&](int& out) -> bool {
+      out = kDqKRing + vs;
+      const bool r = s.wait(ctl->ring_full[kDqKRing + vs], vph, kStatusTimeoutMma);
+      if (++vs == kDqVRing) { vs = 0; vph ^= 1u; }
+      return r;
+    };
+    auto issue_s = [&](int j, int kslot) {
+      ptx::tc_fence_after();
+      if (leader) {
+        mma_kmajor(kTmemBase + col_sbuf(j), L.fixed(0), L.ring(kslot));   // S = Q K^T
+        ptx::mma_commit(s.bar(ctl->sb_full[j & 1]));
+      }
+      __syncwarp();
+    };
+    auto issue_dp = [&](int vslot) {
+      ptx::tc_fence_after();
+      if (leader) {
+        mma_kmajor(kTmemBase + kColDP, L.fixed(1), L.ring(vslot));   // dP = dO V^T
+        ptx::mma_commit(s.bar(ctl->dp_full));
+        ptx::mma_commit(s.bar(ctl->ring_empty[vslot]));
+      }
+      __syncwarp();
+    };
+    int kcur = 0, vslot = 0;
+    ok = ok && next_k(kcur);
+    if (ok) issue_s(0, kcur);
+    ok = ok && next_v(vslot);
+    if (ok) issue_dp(vslot);
     for (int j = 0; ok && j < nkv; ++j) {
-      const int ks = slot;
-      if (!(ok = s.wait(ctl->ring_full[ks], phase, kStatusTimeoutMma))) break;
-      if (++slot == kRing) { slot = 0; phase ^= 1u; }
-      const int vs = slot;
-      if (!(ok = s.wait(ctl->ring_full[vs], phase, kStatusTimeoutMma))) break;
-      if (++slot == kRing) { slot = 0; phase ^= 1u; }
+      const bool more = j + 1 < nkv;
+      int knext = 0;
+      if (more) {
+        if (!(ok = next_k(knext))) break;
+        issue_s(j + 1, knext);
+      }
+      if (!(ok = s.wait(ctl->ds_ready, j & 1u, kStatusTimeoutMma))) break;
       ptx::tc_fence_after();
       if (leader) {
-        mma_kmajor(kTmemBase + kColS, L.fixed(0), L.ring(ks));    // S = Q K^T
-        mma_kmajor(kTmemBase + kColDP, L.fixed(1), L.ring(vs));   // dP = dO V^T
-        ptx::mma_commit(s.bar(ctl->mma_full));
-        ptx::mma_commit(s.bar(ctl->ring_empty[vs]));
+        mma_tmem_a(kTmemBase + kColDQ, kTmemBase + col_sbuf(j) + kColP, L.ring(kcur), j > 0);  // dQ += dS K
+        ptx::mma_commit(s.bar(ctl->ring_empty[kcur]));
+        if (!more) ptx::mma_commit(s.bar(ctl->acc_full));
       }
       __syncwarp();
-      if (!(ok = s.wait(ctl->ew_full, j & 1u, kStatusTimeoutMma))) break;
-      ptx::tc_fence_after();
-      if (leader) {
-        mma_tmem_a(kTmemBase + kColDQ, kTmemBase + kColS + kColP, L.ring(ks), j > 0);  // dQ += dS K
-        ptx::mma_commit(s.bar(ctl->ring_empty[ks]));
-        if (j == nkv - 1) ptx::mma_commit(s.bar(ctl->acc_full));
+      if (more) {
+        if (!(ok = next_v(vslot))) break;
+        issue_dp(vslot);
       }
-      __syncwarp();
+      kcur = knext;
     }
     if (leader) ptx::mma_commit(s.bar(ctl->drain));
     __syncwarp();
@@ -326,35 +423,43 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const uint32_t lane_off = row_base << 16;
     bool ok = true;
     for (int j = 0; ok && j < nkv; ++j) {
-      if (!(ok = s.wait(ctl->mma_full, j & 1u, kStatusTimeoutSoftmax))) break;
+      const uint32_t sb = kTmemBase + lane_off + col_sbuf(j);
+      if (!(ok = s.wait(ctl->sb_full[j & 1], (j >> 1) & 1u, kStatusTimeoutSoftmax))) break;
       ptx::tc_fence_after();
       int valid = kBlockN;
       if (j == p.kv_tiles - 1) valid = p.kv_valid_last;
       if (p.causal && j == qt) valid = min(valid, r + 1);
-      // high chunk first: the packed dS of chunk c lands on S columns 64+16c.., already read
+      // P = exp2(S * scale_log2 - LSE * log2 e), 0 past `valid`; kept in fp32 for dS.
+      float pf[4][32];
 #pragma unroll
-      for (int c = 3; c >= 0; --c) {
-        uint32_t sr[32], dr[32];
-        ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColS + 32 * c, sr);
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32];
+        ptx::tmem_ld_32x32b_x32(sb + 32 * c, sr);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float pv = ptx::ex2_ftz(fmaf(__uint_as_float(sr[i]), p.scale_log2, -lse2));
+          pf[c][i] = 32 * c + i < valid ? pv : 0.f;
+        }
+      }
+      // dS = P o (dP - delta), packed BF16 over the upper half of this S buffer (already read).
+      if (!(ok = s.wait(ctl->dp_full, j & 1u, kStatusTimeoutSoftmax))) break;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t dr[32];
         ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColDP + 32 * c, dr);
         ptx::tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float ds[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int col = 32 * c + 2 * i + h;
-            const float pv = ptx::ex2_ftz(fmaf(__uint_as_float(sr[2 * i + h]), p.scale_log2, -lse2));
-            ds[h] = col < valid ? pv * (__uint_as_float(dr[2 * i + h]) - dlt) : 0.f;
-          }
-          pk[i] = ptx::pack_bf16x2(ds[0], ds[1]);
-        }
-        ptx::tmem_st_32x32b_x16(kTmemBase + lane_off + kColS + kColP + 16 * c, pk);
+        for (int i = 0; i < 16; ++i)
+          pk[i] = ptx::pack_bf16x2(pf[c][2 * i] * (__uint_as_float(dr[2 * i]) - dlt),
+                                   pf[c][2 * i + 1] * (__uint_as_float(dr[2 * i + 1]) - dlt));
+        ptx::tmem_st_32x32b_x16(sb + kColP + 16 * c, pk);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      s.arrive(ctl->ew_full);
+      s.arrive(ctl->ds_ready);
     }
     if (ok && s.wait(ctl->acc_full, 0, kStatusTimeoutSoftmax)) {
       ptx::tc_fence_after();
@@ -401,7 +506,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  const Layout L = setup(smem_raw);
+  const Layout L = setup(smem_raw, kCtlOffsetDkdv);
   SmemCtl* ctl = L.ctl;
   const uint32_t warp = threadIdx.x >> 5;
   Sync s{ctl, threadIdx.x & 31u};
@@ -434,7 +539,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     auto next_slot = [&](int& out) -> bool {
       out = slot;
       const bool r = s.wait(ctl->ring_full[slot], phase, kStatusTimeoutMma);
-      if (++slot == kRing) { slot = 0; phase ^= 1u; }
+      if (++slot == kDkdvRing) { slot = 0; phase ^= 1u; }
       return r;
     };
     int qs = 0, ds = 0;

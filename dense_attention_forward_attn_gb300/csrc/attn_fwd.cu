@@ -56,10 +56,10 @@ int device_info(int dev, DeviceInfo* out) {
   }
   if (!d.bwd_attr_set) {
     if (cudaFuncSetAttribute(attn::bwd::attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(attn::bwd::kSmemBytes)) != cudaSuccess ||
+                             static_cast<int>(attn::bwd::kSmemBytesDq)) != cudaSuccess ||
         cudaFuncSetAttribute(attn::bwd::attn_bwd_dkdv_kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(attn::bwd::kSmemBytes)) != cudaSuccess) {
+                             static_cast<int>(attn::bwd::kSmemBytesDkdv)) != cudaSuccess) {
       cudaGetLastError();
       return ATTN_ERR_CUDA;
     }
@@ -364,11 +364,11 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   p.out0 = dk;
   p.out1 = dv;
   attn::bwd::attn_bwd_dkdv_kernel<<<static_cast<unsigned>(bh * p.kv_tiles), attn::bwd::kThreads,
-                                    attn::bwd::kSmemBytes, st>>>(tm_q, tm_k, tm_v, tm_do, p);
+                                    attn::bwd::kSmemBytesDkdv, st>>>(tm_q, tm_k, tm_v, tm_do, p);
   p.out0 = dq;
   p.out1 = nullptr;
   attn::bwd::attn_bwd_dq_kernel<<<static_cast<unsigned>(bh * p.q_tiles), attn::bwd::kThreads,
-                                  attn::bwd::kSmemBytes, st>>>(tm_q, tm_k, tm_v, tm_do, p);
+                                  attn::bwd::kSmemBytesDq, st>>>(tm_q, tm_k, tm_v, tm_do, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
 }

@@ -198,7 +198,8 @@ int attn_fwd_schedule(int cta, int round, int grid, int64_t work_items, int flag
  * status word.  Bit 0..3: a bounded wait inside the kernel expired (TMA,
  * MMA, softmax, correction role); bit 4: a drain of in-flight work expired;
  * bit 5: the tensor-memory allocation did not start at column 0 (the CTA
- * skipped its work).
+ * skipped its work); bit 6: a backward dQ CTA found its dynamic shared memory
+ * not 1024-byte aligned (it skipped its work).
  * Zero means no kernel since the last reset hit a wait limit.  Synchronous:
  * copies 4 bytes from the device (waits for prior work on the legacy stream).
  */
