@@ -23,8 +23,10 @@
 //     max taken on raw scores, ex2.approx.ftz.
 //   * Chapter 11: the kept row max is replaced only when a tile's max exceeds it
 //     by at least 8 (base-2 units); otherwise P is taken against the stale max.
-//   * Chapter 13: P*V is issued in two parts, K-steps 2..7 once P's upper 96
-//     columns are in TMEM and O is safe, K-steps 0..1 once the lower 32 are.
+//   * Chapter 13 splits P*V to start it before all of P is written; here P*V is
+//     issued whole once P is complete: on GB300 the MMA-issuing warp is the
+//     bottleneck (each tcgen05.mma issue holds it ~50 cycles, each mbarrier wait
+//     ~130), so it waits once for P (and V, polled together) instead of twice.
 //   * Chapter 14: persistent CTAs, one per SM, static stride over work items;
 //     barriers are initialised once and their phases carried across items.
 // LSE = (kept max + log2(row sum)) * ln 2 ("Attention for sm90, Line by Line",
@@ -47,6 +49,7 @@
 #ifndef ATTN_ARRIVE_PER_WARP
 #define ATTN_ARRIVE_PER_WARP 1
 #endif
+
 
 namespace attn {
 
@@ -103,8 +106,7 @@ struct alignas(8) SmemCtl {
   uint64_t q_full[2], q_empty[2];
   uint64_t kv_full[kKvStages], kv_empty[kKvStages];
   uint64_t s_full[2];      // MMA -> softmax: S_q(i) in TMEM
-  uint64_t p_hi_full[2];   // softmax (P cols 32..127) + correction (O safe) -> MMA
-  uint64_t p_lo_full[2];   // softmax (P cols 0..31) -> MMA
+  uint64_t p_full[2];      // softmax (P in TMEM) + correction (O rescaled or untouched) -> MMA
   uint64_t stats_full[2];  // softmax -> correction: per-row rescale factor published
   uint64_t o_full[2];      // MMA -> correction: last P*V of the item done
   // softmax -> correction: final row max / row sum of an item published, one barrier per item
@@ -247,6 +249,27 @@ struct Ctx {
     }
   }
 
+  // Two barriers at once: both try_waits are in flight together, so their latencies overlap.
+  __device__ bool wait2(const uint64_t& b1, uint32_t par1, const uint64_t& b2, uint32_t par2,
+                        unsigned role_bit) const {
+    const uint32_t a1 = bar(b1), a2 = bar(b2);
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (true) {
+      const uint32_t r1 = ptx::mbar_try_wait(a1, par1);
+      const uint32_t r2 = ptx::mbar_try_wait(a2, par2);
+      if (__all_sync(0xffffffffu, r1 & r2)) return true;
+      const bool stop = ctl->abort_flag != 0 || (ptx::globaltimer_ns() - t0) > kWaitLimitNs;
+      if (__any_sync(0xffffffffu, stop)) {
+        if (lane == 0) {
+          ctl->abort_flag = 1;
+          atomicOr(&g_attn_status, role_bit);
+        }
+        __syncwarp();
+        return false;
+      }
+    }
+  }
+
   // Bounded wait on this warp's own in-flight work, ignoring the abort flag.
   __device__ void drain_wait(const uint64_t& b, uint32_t parity) const {
     const uint32_t addr = bar(b);
@@ -343,16 +366,16 @@ __device__ __forceinline__ void issue_qk(const Ctx& c, int kslot) {
   }
 }
 
-// K-steps [K0, K1) of P_q * V: A = packed P in TMEM, B = V tile (MN-major, 128B swizzle).
-template <int Q, int K0, int K1>
+// P_q * V: A = packed P in TMEM, B = V tile (MN-major, 128B swizzle), 8 K-steps of 16 keys.
+template <int Q>
 __device__ __forceinline__ void issue_pv(const Ctx& c, int vslot, bool overwrite_first) {
   constexpr uint32_t idesc = make_idesc_bf16(128, 128, 1);
   const uint64_t b0 = smem_desc_sw128(c.skv(vslot), kSlabBytes, 1024);
 #pragma unroll
-  for (int kk = K0; kk < K1; ++kk) {
+  for (int kk = 0; kk < 8; ++kk) {
     // 16 V rows per K-step: 16 * 128 bytes inside each 64-column slab.
     ptx::mma_ts(kTmemBase + col_o(Q), kTmemBase + col_s(Q) + kColP + kk * 8,
-                b0 + ((kk * 16 * 128) >> 4), idesc, (kk == K0 && overwrite_first) ? 0u : 1u);
+                b0 + ((kk * 16 * 128) >> 4), idesc, (kk == 0 && overwrite_first) ? 0u : 1u);
   }
 }
 
@@ -387,17 +410,20 @@ __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
     __syncwarp();
     return true;
   };
-  auto pv = [&](int q, int vslot, bool first_tile) -> bool {
-    if (!c.wait(ctl->p_hi_full[q], pv_phase[q], kStatusTimeoutMma)) return false;
-    ptx::tc_fence_after();
-    if (leader) {
-      if (q == 0) issue_pv<0, 2, 8>(c, vslot, first_tile); else issue_pv<1, 2, 8>(c, vslot, first_tile);
+  // P_q V with V in vslot.  v_phase >= 0: V's token is waited for here too, in the same poll as P
+  // (a wait on an mbarrier costs this warp about as much as two MMA issues, and the MMA warp's
+  // own instruction time bounds the pipeline, so it waits as rarely as it can).
+  auto pv = [&](int q, int vslot, bool first_tile, int v_phase) -> bool {
+    if (v_phase >= 0) {
+      if (!c.wait2(ctl->kv_full[vslot], static_cast<uint32_t>(v_phase), ctl->p_full[q],
+                   pv_phase[q], kStatusTimeoutMma))
+        return false;
+    } else if (!c.wait(ctl->p_full[q], pv_phase[q], kStatusTimeoutMma)) {
+      return false;
     }
-    __syncwarp();
-    if (!c.wait(ctl->p_lo_full[q], pv_phase[q], kStatusTimeoutMma)) return false;
     ptx::tc_fence_after();
     if (leader) {
-      if (q == 0) issue_pv<0, 0, 2>(c, vslot, false); else issue_pv<1, 0, 2>(c, vslot, false);
+      if (q == 0) issue_pv<0>(c, vslot, first_tile); else issue_pv<1>(c, vslot, first_tile);
     }
     __syncwarp();
     pv_phase[q] ^= 1u;
@@ -430,12 +456,15 @@ __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
       };
       bool next0_done = false;
       for (int j = 0; ok && j < ntiles; ++j) {
-        int vslot;
-        if (!(ok = next_kv(vslot))) break;
+        // V(j): its token is taken from the ring here and waited for by the first P V on it.
+        const int vslot = slot;
+        int v_phase = static_cast<int>(phase);
+        if (++slot == kKvStages) { slot = 0; phase ^= 1u; }
         int kslot_next = -1;
         // stage 0: P0 V(j), then Q0 K(j+1)
         if (j < w.n[0]) {
-          if (!(ok = pv(0, vslot, j == 0))) break;
+          if (!(ok = pv(0, vslot, j == 0, v_phase))) break;
+          v_phase = -1;
           if (leader) {
             if (j == w.n[0] - 1) ptx::mma_commit(c.bar(ctl->o_full[0]));
             if (j >= w.n[1]) ptx::mma_commit(c.bar(ctl->kv_empty[vslot]));
@@ -451,7 +480,8 @@ __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
         }
         // stage 1: P1 V(j), then Q1 K(j+1)
         if (j < w.n[1]) {
-          if (!(ok = pv(1, vslot, j == 0))) break;
+          if (!(ok = pv(1, vslot, j == 0, v_phase))) break;
+          v_phase = -1;
           if (leader) {
             if (j == w.n[1] - 1) ptx::mma_commit(c.bar(ctl->o_full[1]));
             ptx::mma_commit(c.bar(ctl->kv_empty[vslot]));
@@ -492,9 +522,9 @@ __device__ __forceinline__ void mask_scores(uint32_t (&sr)[4][32], int valid, ui
 }
 
 // P of one KV tile: exp2(s * scale_log2 - m_kept), two columns per packed FMA, packed BF16 into
-// TMEM over the upper half of this stage's S columns; the upper 96 columns are published first
-// (p_hi_full: P*V K-steps 2..7 may start), then the lower 32 (p_lo_full).  Masked columns arrive
-// as -inf and come out as 0.  Returns the row sum of the tile's fp32 P.
+// TMEM over the upper half of this stage's S columns, published once all 128 are written
+// (p_full).  Masked columns arrive as -inf and come out as 0.  Returns the row sum of the tile's
+// fp32 P.
 __device__ __forceinline__ float produce_p(const Ctx& c, int q, const uint32_t (&sr)[4][32],
                                            float scale_log2, float m_kept, uint32_t taddr_s) {
   SmemCtl* ctl = c.ctl;
@@ -516,15 +546,10 @@ __device__ __forceinline__ float produce_p(const Ctx& c, int q, const uint32_t (
     }
     sum2[cc] = ptx::fadd2(acc0, acc1);
     ptx::tmem_st_32x32b_x16(taddr_s + kColP + 16 * cc, pk);
-    if (cc == 1) {
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      c.arrive(ctl->p_hi_full[q]);
-    }
   }
   ptx::tmem_wait_st();
   ptx::tc_fence_before();
-  c.arrive(ctl->p_lo_full[q]);
+  c.arrive(ctl->p_full[q]);
   const float2 t2 = ptx::fadd2(ptx::fadd2(sum2[3], sum2[2]), ptx::fadd2(sum2[1], sum2[0]));
   return t2.x + t2.y;
 }
@@ -686,7 +711,7 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
           ptx::tmem_wait_st();
         }
         ptx::tc_fence_before();
-        c.arrive(ctl->p_hi_full[q]);
+        c.arrive(ctl->p_full[q]);
         tphase[q] ^= 1u;
       }
     }
@@ -721,8 +746,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ptx::mbar_init(c.bar(ctl->q_full[q]), 1);
       ptx::mbar_init(c.bar(ctl->q_empty[q]), 1);
       ptx::mbar_init(c.bar(ctl->s_full[q]), 1);
-      ptx::mbar_init(c.bar(ctl->p_hi_full[q]), 2 * kArrivePerWG);   // softmax + correction WGs
-      ptx::mbar_init(c.bar(ctl->p_lo_full[q]), kArrivePerWG);
+      ptx::mbar_init(c.bar(ctl->p_full[q]), 2 * kArrivePerWG);   // softmax + correction WGs
       ptx::mbar_init(c.bar(ctl->stats_full[q]), kArrivePerWG);
       ptx::mbar_init(c.bar(ctl->o_full[q]), 1);
       ptx::mbar_init(c.bar(ctl->final_full[q][0]), kArrivePerWG);
