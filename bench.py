@@ -319,7 +319,8 @@ def run_ours(args):
                            "tflops": round(flop_factor * w.flops / (avg * 1e-3) / 1e12, 1)}
     status = attn.device_status()
 
-    # ---------------- end to end through the public API with host buffers (forward rows)
+    # ---------------- end to end with host buffers (forward rows): attn.fwd on pinned CPU tensors
+    # runs attn_fwd_host, the C-ABI entry point that copies in chunks overlapped with the kernel
     e2e = None
     if not backward:
         h2d = sum(sum(t.numel() * t.element_size() for t in host) for _, _, host, *_ in shapes)

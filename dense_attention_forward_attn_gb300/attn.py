@@ -39,7 +39,8 @@ class _Plan(ctypes.Structure):
                 ("smem_bytes", ctypes.c_int), ("tmem_cols", ctypes.c_int)]
 
 
-EXPORTS = ("attn_fwd", "attn_fwd_ex", "attn_bwd", "attn_bwd_noalloc", "attn_status_string",
+EXPORTS = ("attn_fwd", "attn_fwd_ex", "attn_fwd_host", "attn_fwd_host_workspace",
+           "attn_fwd_host_chunking", "attn_bwd", "attn_bwd_noalloc", "attn_status_string",
            "attn_fwd_plan", "attn_fwd_work_item", "attn_fwd_schedule", "attn_device_status")
 
 
@@ -53,6 +54,14 @@ def _bind(lib):
     lib.attn_fwd.restype = i32
     lib.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp]
     lib.attn_fwd_ex.restype = i32
+    sz = ctypes.c_size_t
+    lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
+    lib.attn_fwd_host.restype = i32
+    lib.attn_fwd_host_workspace.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
+    lib.attn_fwd_host_workspace.restype = i32
+    lib.attn_fwd_host_chunking.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(i64),
+                                           ctypes.POINTER(i64)]
+    lib.attn_fwd_host_chunking.restype = i32
     lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32,
                              i32, vp]
     lib.attn_bwd.restype = i32
@@ -124,6 +133,18 @@ def schedule(cta: int, rnd: int, grid: int, work_items: int, causal: bool = Fals
     return int(library().attn_fwd_schedule(cta, rnd, grid, work_items, _flags(causal)))
 
 
+def host_chunking(B: int, H: int, Sq: int, Sk: int, num_sms: int, causal: bool = False,
+                  layout: str = "bhsd"):
+    """(units per chunk, chunks) of the host-buffer forward; units are heads ([B,H,S,D]) or
+    batch entries ([B,S,H,D]); the last chunk takes the remainder."""
+    per, n = ctypes.c_int64(), ctypes.c_int64()
+    rc = library().attn_fwd_host_chunking(B, H, Sq, Sk, _flags(causal, layout), num_sms,
+                                          ctypes.byref(per), ctypes.byref(n))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_host_chunking")
+    return per.value, n.value
+
+
 def device_status(clear: bool = False) -> int:
     w = ctypes.c_uint(0)
     rc = library().attn_device_status(ctypes.byref(w), 1 if clear else 0)
@@ -184,29 +205,50 @@ def fwd(q, k, v, scale: float | None = None, return_lse: bool = True, causal: bo
     BF16 contiguous.  Returns (o in q's layout, lse [B,H,Sq] or None).
 
     CUDA tensors: runs on the current stream, returns (o, lse) on the device.
-    CPU tensors: copies the inputs to the current CUDA device (pinned host
-    memory, asynchronous), runs, copies O and LSE back and returns CPU tensors.
+    CPU tensors: attn_fwd_host -- the library copies the inputs to the current
+    CUDA device in chunks (pinned host memory, pinned here first if needed),
+    overlapping the copies with the kernel, copies O and LSE back into pinned
+    CPU tensors and this call returns them once they are complete.
     """
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _check(t, n)
-    host = not q.is_cuda
-    if host:
-        dev = torch.device("cuda", torch.cuda.current_device())
-        q, k, v = (t.pin_memory().to(dev, non_blocking=True) for t in (q, k, v))
-    B, H, Sq, _, D = _dims(q, k, layout)
+    B, H, Sq, Sk, D = _dims(q, k, layout)
+    if not q.is_cuda:
+        return _fwd_host(q, k, v, B, H, Sq, Sk, D, scale, return_lse, causal, layout)
     o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device) if return_lse else None
     fwd_into(q, k, v, o, lse, scale, causal=causal, layout=layout)
-    if host:
-        o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-        o_h.copy_(o, non_blocking=True)
-        lse_h = None
-        if lse is not None:
-            lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-            lse_h.copy_(lse, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-        return o_h, lse_h
+    return o, lse
+
+
+def _fwd_host(q, k, v, B, H, Sq, Sk, D, scale, return_lse, causal, layout):
+    import torch
+    if k.is_cuda or v.is_cuda:
+        raise ValueError("q, k, v must all be CPU tensors or all CUDA tensors")
+    kv_shape = (B, Sk, H, D) if layout == "bshd" else (B, H, Sk, D)
+    if tuple(k.shape) != kv_shape or tuple(v.shape) != kv_shape:
+        raise ValueError("shape mismatch between q, k, v")
+    flags = _flags(causal, layout)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    q, k, v = (t if t.is_pinned() else t.pin_memory() for t in (q, k, v))
+    lib = library()
+    ws = ctypes.c_size_t()
+    rc = lib.attn_fwd_host_workspace(B, H, Sq, Sk, D, flags, ctypes.byref(ws))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_host_workspace")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    work = torch.empty(max(ws.value, 1), dtype=torch.uint8, device=dev)
+    o = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True)
+    lse = torch.empty((B, H, Sq), dtype=torch.float32, pin_memory=True) if return_lse else None
+    stream = torch.cuda.current_stream(dev)
+    rc = lib.attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           lse.data_ptr() if lse is not None else None, B, H, Sq, Sk, D,
+                           float(scale), flags, work.data_ptr(), ws.value, stream.cuda_stream)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_host")
+    stream.synchronize()
     return o, lse
 
 

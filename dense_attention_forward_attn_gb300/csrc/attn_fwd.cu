@@ -12,6 +12,7 @@
 #include "../../include/attn_fwd.h"
 #include "attn_fwd_kernel.cuh"
 #include "attn_bwd_kernel.cuh"
+#include "attn_host.cuh"
 
 namespace {
 
@@ -277,6 +278,150 @@ int attn_device_status(unsigned int* word, int clear) {
       return ATTN_ERR_CUDA;
     }
   }
+  return ATTN_OK;
+}
+
+// ------------------------------------------------------------------ host-buffer forward
+namespace {
+attn::host::Pipe g_pipe[kMaxDevices];
+std::mutex g_pipe_mu;
+
+int host_shape(int B, int H, int Sq, int Sk, int D, int flags) {
+  if (flags & ~ATTN_FLAGS_ALL) return ATTN_ERR_INVALID_ARG;
+  return check_shape(B, H, Sq, Sk, D);
+}
+
+// Lazily create the two copy streams and the events of this device (under g_pipe_mu).
+int pipe_for(int dev, attn::host::Pipe** out) {
+  attn::host::Pipe& P = g_pipe[dev];
+  if (!P.ready) {
+    bool ok = cudaStreamCreateWithFlags(&P.in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&P.out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&P.start, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < attn::host::kMaxChunks; ++i)
+      ok = cudaEventCreateWithFlags(&P.ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&P.ev_k[i], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&P.ev_out[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    P.ready = true;
+  }
+  *out = &P;
+  return ATTN_OK;
+}
+}  // namespace
+
+int attn_fwd_host_workspace(int B, int H, int Sq, int Sk, int D, int flags, size_t* bytes) {
+  if (bytes == nullptr) return ATTN_ERR_INVALID_ARG;
+  const int rc = host_shape(B, H, Sq, Sk, D, flags);
+  if (rc != ATTN_OK) return rc;
+  *bytes = attn::host::layout(static_cast<int64_t>(B) * H, Sq, Sk, D).total;
+  return ATTN_OK;
+}
+
+int attn_fwd_host_chunking(int B, int H, int Sq, int Sk, int flags, int num_sms,
+                           int64_t* units_per_chunk, int64_t* chunks) {
+  if (units_per_chunk == nullptr || chunks == nullptr || num_sms <= 0) return ATTN_ERR_INVALID_ARG;
+  const int rc = host_shape(B, H, Sq, Sk, attn::kHeadDim, flags);
+  if (rc != ATTN_OK) return rc;
+  const bool bshd = (flags & ATTN_FLAG_BSHD) != 0;
+  const int64_t pairs = (ceil_div(Sq, attn::kBlockM) + 1) / 2;
+  const int64_t units = bshd ? B : static_cast<int64_t>(B) * H;
+  const int64_t per_unit = bshd ? static_cast<int64_t>(H) * pairs : pairs;
+  const int64_t items = units * per_unit;
+  const int64_t grid = items < num_sms ? items : num_sms;
+  if (units == 0) {
+    *units_per_chunk = *chunks = 0;
+    return ATTN_OK;
+  }
+  *units_per_chunk = attn::host::host_chunk_units(units, per_unit, grid, attn::host::kMaxChunks);
+  *chunks = (units + *units_per_chunk - 1) / *units_per_chunk;
+  return ATTN_OK;
+}
+
+int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                  int Sq, int Sk, int D, float scale, int flags, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  int rc = host_shape(B, H, Sq, Sk, D, flags);
+  if (rc != ATTN_OK) return rc;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (scale < 0.f) return ATTN_ERR_UNSUPPORTED;
+  const int64_t bh = static_cast<int64_t>(B) * H;
+  if (bh == 0 || Sq == 0) return ATTN_OK;
+  if (!q || !k || !v || !o || !workspace) return ATTN_ERR_INVALID_ARG;
+  const attn::host::Layout L = attn::host::layout(bh, Sq, Sk, D);
+  if (workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return ATTN_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  DeviceInfo info;
+  rc = device_info(dev, &info);
+  if (rc != ATTN_OK) return rc;
+  int64_t per_chunk = 0, nchunks = 0;
+  rc = attn_fwd_host_chunking(B, H, Sq, Sk, flags, info.num_sms, &per_chunk, &nchunks);
+  if (rc != ATTN_OK) return rc;
+
+  const bool bshd = (flags & ATTN_FLAG_BSHD) != 0;
+  // bytes of one unit (a head, or a batch entry) of each tensor
+  const size_t uq = static_cast<size_t>(Sq) * D * 2 * (bshd ? H : 1);
+  const size_t uk = static_cast<size_t>(Sk) * D * 2 * (bshd ? H : 1);
+  const size_t ul = static_cast<size_t>(Sq) * 4 * (bshd ? H : 1);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+
+  std::lock_guard<std::mutex> lk(g_pipe_mu);
+  attn::host::Pipe* P = nullptr;
+  rc = pipe_for(dev, &P);
+  if (rc != ATTN_OK) return rc;
+  auto fail = [] {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  };
+  // The copies start after everything already queued on the caller's stream (which may still
+  // read the workspace, or write these host buffers).
+  if (cudaEventRecord(P->start, cs) != cudaSuccess ||
+      cudaStreamWaitEvent(P->in, P->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(P->out, P->start, 0) != cudaSuccess)
+    return fail();
+  const int64_t units = bshd ? B : bh;
+  for (int64_t c = 0, u0 = 0; c < nchunks; ++c) {
+    const int64_t nu = units - u0 < per_chunk ? units - u0 : per_chunk;
+    uint8_t* dq = ws + L.q + u0 * uq;
+    uint8_t* dk = ws + L.k + u0 * uk;
+    uint8_t* dv = ws + L.v + u0 * uk;
+    uint8_t* dO = ws + L.o + u0 * uq;
+    float* dl = lse ? reinterpret_cast<float*>(ws + L.lse + u0 * ul) : nullptr;
+    const uint8_t* hq = static_cast<const uint8_t*>(q) + u0 * uq;
+    const uint8_t* hk = static_cast<const uint8_t*>(k) + u0 * uk;
+    const uint8_t* hv = static_cast<const uint8_t*>(v) + u0 * uk;
+    if (cudaMemcpyAsync(dq, hq, nu * uq, cudaMemcpyHostToDevice, P->in) != cudaSuccess ||
+        cudaMemcpyAsync(dk, hk, nu * uk, cudaMemcpyHostToDevice, P->in) != cudaSuccess ||
+        cudaMemcpyAsync(dv, hv, nu * uk, cudaMemcpyHostToDevice, P->in) != cudaSuccess ||
+        cudaEventRecord(P->ev_in[c], P->in) != cudaSuccess ||
+        cudaStreamWaitEvent(cs, P->ev_in[c], 0) != cudaSuccess)
+      return fail();
+    const int sub_b = bshd ? static_cast<int>(nu) : 1;
+    const int sub_h = bshd ? H : static_cast<int>(nu);
+    rc = attn_fwd_ex(dq, dk, dv, dO, dl, sub_b, sub_h, Sq, Sk, D, scale, flags, stream);
+    if (rc != ATTN_OK) return rc;
+    if (cudaEventRecord(P->ev_k[c], cs) != cudaSuccess ||
+        cudaStreamWaitEvent(P->out, P->ev_k[c], 0) != cudaSuccess ||
+        cudaMemcpyAsync(static_cast<uint8_t*>(o) + u0 * uq, dO, nu * uq, cudaMemcpyDeviceToHost,
+                        P->out) != cudaSuccess)
+      return fail();
+    if (lse && cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse) + u0 * ul, dl, nu * ul,
+                               cudaMemcpyDeviceToHost, P->out) != cudaSuccess)
+      return fail();
+    if (cudaEventRecord(P->ev_out[c], P->out) != cudaSuccess) return fail();
+    u0 += nu;
+  }
+  // The caller's stream completes only after the last copy back (the out stream is in order).
+  if (cudaStreamWaitEvent(cs, P->ev_out[nchunks - 1], 0) != cudaSuccess) return fail();
   return ATTN_OK;
 }
 

@@ -24,6 +24,7 @@
 #ifndef ATTN_FWD_H_
 #define ATTN_FWD_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -97,6 +98,52 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  */
 int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                 int Sq, int Sk, int D, float scale, int flags, void* stream);
+
+/*
+ * attn_fwd_host -- attn_fwd_ex with Q/K/V read from and O/LSE written to HOST
+ * memory.  The pages' kernels take device tensors; this entry point is the
+ * library's own end-to-end path for inputs that start on the host.
+ *
+ *   q, k, v     host, BF16, layout per flags as attn_fwd_ex (read)
+ *   o           host, BF16, q's shape (written)
+ *   lse         host, fp32, [B, H, Sq] (written) or NULL
+ *   workspace   device memory owned by the caller, 256-byte aligned, at least
+ *               attn_fwd_host_workspace() bytes; holds the device copies of
+ *               q, k, v, o, lse; contents on entry are ignored
+ *   stream      the caller's stream; the kernels run on it, the copies on two
+ *               internal streams of the library that wait for the work already
+ *               queued on it, and it waits for the last copy back
+ *
+ * The problem is split into chunks of whole heads ([B,H,S,D]) or whole batch
+ * entries ([B,S,H,D]); each chunk's host-to-device copy, kernel and copy back
+ * are ordered by events so chunks overlap one another.  Host buffers should be
+ * page-locked (cudaHostAlloc / pinned) for the copies to be asynchronous;
+ * pageable memory works but the copies then block the calling thread.  o and lse
+ * hold the result once `stream` has completed the call's work.  The workspace
+ * must not be used by other work until then.  Sizes, scale, flags and errors
+ * as attn_fwd_ex, plus ATTN_ERR_INVALID_ARG for a NULL or short or misaligned
+ * workspace.  Calls from several threads are serialised while they enqueue.
+ */
+int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                  int Sq, int Sk, int D, float scale, int flags, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/*
+ * attn_fwd_host_workspace -- bytes of device workspace attn_fwd_host needs for
+ * this problem (written to *bytes).  Host only; errors as attn_fwd_ex's checks.
+ */
+int attn_fwd_host_workspace(int B, int H, int Sq, int Sk, int D, int flags, size_t* bytes);
+
+/*
+ * attn_fwd_host_chunking -- how attn_fwd_host splits the problem for a device of
+ * num_sms SMs: chunks of *units_per_chunk heads ([B,H,S,D]) or batch entries
+ * ([B,S,H,D]), the last one shorter if they do not divide evenly; *chunks in
+ * all, at most 8.  The chunk size is chosen so the chunks' work items fill whole
+ * rounds of the persistent grid where possible, with more chunks (more overlap
+ * of copies and kernels) breaking ties.  Host only.
+ */
+int attn_fwd_host_chunking(int B, int H, int Sq, int Sk, int flags, int num_sms,
+                           int64_t* units_per_chunk, int64_t* chunks);
 
 /*
  * attn_bwd -- enqueue the backward of attn_fwd(_ex) on `stream`: given the

@@ -328,3 +328,46 @@ def test_bshd_full_size_sampled_rows():
     o_bhsd = o2.float().cpu().numpy().astype(np.float64).reshape(-1, w.Sq, w.D)
     _assert_close(o_bhsd[bh, rows], o_ref, lse.cpu().numpy().astype(np.float64).reshape(-1, w.Sq)[bh, rows],
                   lse_ref)
+
+
+# ------------------------------------------------------------- host buffers (attn_fwd_host)
+
+@pytest.mark.parametrize("shape,causal,layout,with_lse", [
+    ((2, 40, 1024, 1024), False, "bhsd", True),    # several chunks of heads
+    ((3, 5, 300, 700), True, "bhsd", True),
+    ((9, 3, 640, 640), False, "bshd", True),       # chunks of batch entries
+    ((1, 4, 256, 128), False, "bhsd", False),
+])
+def test_host_buffer_forward_matches_device_path(shape, causal, layout, with_lse):
+    B, H, Sq, Sk = shape
+    qb, kb, vb = wl.make_inputs_bits(B, H, Sq, Sk, 128, seed=41)
+    tens = [wl.bits_to_torch(x) for x in (qb, kb, vb)]
+    if layout == "bshd":
+        tens = [t.transpose(1, 2).contiguous() for t in tens]
+    o_h, lse_h = attn.fwd(*tens, scale=0.1, causal=causal, layout=layout, return_lse=with_lse)
+    assert not o_h.is_cuda and o_h.is_pinned()
+    o_d, lse_d = attn.fwd(*(t.cuda() for t in tens), scale=0.1, causal=causal, layout=layout)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o_d.cpu())
+    if with_lse:
+        assert torch.equal(lse_h, lse_d.cpu())
+    else:
+        assert lse_h is None
+    assert attn.device_status() == 0
+
+
+def test_host_buffer_forward_full_size():
+    """S=4K (B=4, H=16) from host memory: chunks of 19/19/19/7 heads; bitwise equal to the
+    device path, sampled rows against the oracle."""
+    w = wl.S4K
+    qb, kb, vb = wl.workload_inputs_bits(w)
+    tens = [wl.bits_to_torch(x).pin_memory() for x in (qb, kb, vb)]
+    o_h, lse_h = attn.fwd(*tens, scale=w.scale)
+    o_d, lse_d = attn.fwd(*(t.cuda() for t in tens), scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
+    bh, rows = _rows_sample(w, 100, seed=9)
+    o_ref, lse_ref = oracle.attn_fwd_rows(qb, kb, vb, w.scale, bh, rows)
+    o64 = o_h.float().numpy().astype(np.float64).reshape(-1, w.Sq, w.D)
+    _assert_close(o64[bh, rows], o_ref, lse_h.numpy().astype(np.float64).reshape(-1, w.Sq)[bh, rows],
+                  lse_ref)

@@ -199,3 +199,40 @@ def test_schedule_covers_every_item_once(lib):
     # dense: static stride; causal: every other round reversed
     assert [attn.schedule(0, r, 148, 2048) for r in range(3)] == [0, 148, 296]
     assert [attn.schedule(0, r, 148, 2048, causal=True) for r in range(3)] == [0, 295, 296]
+
+
+# ------------------------------------------------------------- host-buffer forward planning
+
+@pytest.mark.parametrize("B,H,S,expect", [
+    (4, 16, 4096, (19, 4)),    # 16 items per head: 19 heads = 2 full rounds of 152
+    (2, 16, 8192, (14, 3)),    # 32 per head: 14 heads = 448 items, 3 rounds
+    (1, 16, 16384, (7, 3)),    # 64 per head: 7 heads = 448 items
+])
+def test_host_chunking_headline_shapes(lib, B, H, S, expect):
+    per, n = attn.host_chunking(B, H, S, S, 152)
+    assert (per, n) == expect
+    # the chunked launches need no more grid rounds than one launch over everything
+    units, per_unit = B * H, S // 256
+    rounds = sum(-(-(min(per, units - u) * per_unit) // 152) for u in range(0, units, per))
+    assert rounds == -(-(units * per_unit) // 152)
+
+
+@pytest.mark.parametrize("B,H,Sq,Sk,layout,causal", [
+    (1, 1, 128, 128, "bhsd", False), (3, 7, 300, 500, "bhsd", True), (2, 40, 1024, 1024, "bhsd", False),
+    (4, 16, 4096, 4096, "bshd", False), (1, 200, 256, 128, "bhsd", False), (9, 3, 640, 640, "bshd", True),
+])
+def test_host_chunking_properties(lib, B, H, Sq, Sk, layout, causal):
+    per, n = attn.host_chunking(B, H, Sq, Sk, 152, causal=causal, layout=layout)
+    units = B if layout == "bshd" else B * H
+    assert 1 <= n <= 8 and 1 <= per <= units
+    assert per * n >= units and per * (n - 1) < units
+
+
+def test_host_workspace_bytes(lib):
+    ws = ctypes.c_size_t()
+    assert lib.attn_fwd_host_workspace(2, 3, 300, 500, 128, 0, ctypes.byref(ws)) == attn.ATTN_OK
+    al = lambda x: (x + 255) // 256 * 256
+    q, kv, l = 6 * 300 * 128 * 2, 6 * 500 * 128 * 2, 6 * 300 * 4
+    assert ws.value == al(q) + 2 * al(kv) + al(q) + al(l)
+    assert lib.attn_fwd_host_workspace(2, 3, 300, 500, 64, 0, ctypes.byref(ws)) == attn.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_fwd_host_workspace(2, 3, 300, 500, 128, 8, ctypes.byref(ws)) == attn.ATTN_ERR_INVALID_ARG
