@@ -252,15 +252,21 @@ def _fwd_host(q, k, v, B, H, Sq, Sk, D, scale, return_lse, causal, layout):
     return o, lse
 
 
-def bwd(q, k, v, o, dout, lse, scale: float | None = None, causal: bool = False):
-    """Backward of fwd (device tensors, [B,H,S,D] BF16; lse [B,H,Sq] fp32 from fwd).
+def bwd(q, k, v, o, dout, lse, scale: float | None = None, causal: bool = False,
+        layout: str = "bhsd"):
+    """Backward of fwd (device tensors, BF16; layout "bhsd": q/o/dout [B,H,Sq,D], k/v [B,H,Sk,D];
+    "bshd": [B,S,H,D]; lse [B,H,Sq] fp32 from fwd either way).
 
     Returns (dq, dk, dv), BF16 in the shapes of q, k, v.  Runs on the current stream.
     """
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
         _check(t, n)
-    B, H, Sq, Sk, D = _dims(q, k, "bhsd")
+    flags = _flags(causal, layout)
+    B, H, Sq, Sk, D = _dims(q, k, layout)
+    kv_shape = (B, Sk, H, D) if layout == "bshd" else (B, H, Sk, D)
+    if tuple(v.shape) != kv_shape or tuple(k.shape) != kv_shape:
+        raise ValueError("k and v must have the same shape")
     if tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
         raise ValueError("o and dout must have q's shape")
     if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Sq) or not lse.is_contiguous():
@@ -274,7 +280,7 @@ def bwd(q, k, v, o, dout, lse, scale: float | None = None, causal: bool = False)
     stream = torch.cuda.current_stream(q.device).cuda_stream
     rc = library().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
                             lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                            delta.data_ptr(), B, H, Sq, Sk, D, float(scale), _flags(causal), stream)
+                            delta.data_ptr(), B, H, Sq, Sk, D, float(scale), flags, stream)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_bwd")
     return dq, dk, dv

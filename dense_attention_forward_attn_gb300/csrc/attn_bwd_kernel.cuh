@@ -46,6 +46,8 @@ struct Params {
   int q_tiles, kv_tiles;
   int q_valid_last, kv_valid_last;   // valid rows in the last Q / K/V tile, 1..128
   int bh;
+  int heads;           // H
+  int bshd;            // 1: Q/K/V/dO and the gradients are [B,S,H,D] (lse, delta stay [B,H,S])
   int causal;
   float scale;         // softmax scale
   float scale_log2;    // scale * log2(e)
@@ -121,15 +123,23 @@ struct Sync {
 };
 
 // ------------------------------------------------------------------ delta = rowsum(dO o O)
+// delta[row] for rows in [B,H,Sq] order; O and dO are [B,H,Sq,128] or, with bshd, [B,Sq,H,128].
 __global__ void __launch_bounds__(256) attn_bwd_delta_kernel(const uint16_t* __restrict__ o,
                                                              const uint16_t* __restrict__ dout,
                                                              float* __restrict__ delta,
-                                                             int64_t rows) {
+                                                             int64_t rows, int heads, int sq,
+                                                             int bshd) {
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const uint32_t lane = threadIdx.x & 31u;
   if (row >= rows) return;
-  const uint2 a = *reinterpret_cast<const uint2*>(o + row * kHeadDim + lane * 4);
-  const uint2 b = *reinterpret_cast<const uint2*>(dout + row * kHeadDim + lane * 4);
+  int64_t src = row;
+  if (bshd) {
+    const int64_t bh = row / sq, s = row - bh * sq;
+    const int64_t b = bh / heads, h = bh - b * heads;
+    src = (b * sq + s) * heads + h;
+  }
+  const uint2 a = *reinterpret_cast<const uint2*>(o + src * kHeadDim + lane * 4);
+  const uint2 b = *reinterpret_cast<const uint2*>(dout + src * kHeadDim + lane * 4);
   auto lo = [](uint32_t x) { return __uint_as_float(x << 16); };
   auto hi = [](uint32_t x) { return __uint_as_float(x & 0xffff0000u); };
   float acc = lo(a.x) * lo(b.x);
@@ -165,11 +175,28 @@ __device__ __forceinline__ void mma_tmem_a(uint32_t d, uint32_t a, uint32_t b_sm
                 (accumulate || kk > 0) ? 1u : 0u);
 }
 
-// Load two 64-column boxes (one 128-row tile) of a [B*H, S, 128] tensor map.
+// Load two 64-column boxes (one 128-row tile) of head bh: from the 3-D map (128, S, B*H) of a
+// [B,H,S,128] tensor (heads4d == 0) or the 4-D map (128, H, S, B) of a [B,S,H,128] tensor
+// (heads4d == H).
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* tm, uint32_t bar,
-                                          int row, int bh) {
-  ptx::tma_load_3d(dst, tm, bar, 0, row, bh);
-  ptx::tma_load_3d(dst + kSlabBytes, tm, bar, 64, row, bh);
+                                          int row, int bh, int heads4d) {
+  if (heads4d) {
+    const int b = bh / heads4d, h = bh - b * heads4d;
+    ptx::tma_load_4d(dst, tm, bar, 0, h, row, b);
+    ptx::tma_load_4d(dst + kSlabBytes, tm, bar, 64, h, row, b);
+  } else {
+    ptx::tma_load_3d(dst, tm, bar, 0, row, bh);
+    ptx::tma_load_3d(dst + kSlabBytes, tm, bar, 64, row, bh);
+  }
+}
+
+// Byte offset of row `row` of head bh in a BF16 [B,H,S,128] or [B,S,H,128] tensor.
+__device__ __forceinline__ size_t row_offset(const Params& p, int bh, int row, int seq) {
+  if (p.bshd) {
+    const int b = bh / p.heads, h = bh - b * p.heads;
+    return ((static_cast<size_t>(b) * seq + row) * p.heads + h) * (kHeadDim * 2);
+  }
+  return (static_cast<size_t>(bh) * seq + row) * (kHeadDim * 2);
 }
 
 // Write 16 fp32 accumulator columns as BF16 (times `mul`) to a global row.
@@ -189,14 +216,16 @@ __device__ __forceinline__ void zero_row(uint8_t* out) {
 
 struct Layout {
   SmemCtl* ctl;
+  int heads4d;     // H for [B,S,H,D] tensors (4-D tensor maps), 0 for [B,H,S,D]
   uint32_t base;   // 1024-aligned shared address of the first resident tile
   __device__ uint32_t fixed(int i) const { return base + i * kTileBytes; }
   __device__ uint32_t ring(int s) const { return base + (2 + s) * kTileBytes; }
 };
 
-__device__ __forceinline__ Layout setup(uint8_t* smem_raw, uint32_t ctl_offset) {
+__device__ __forceinline__ Layout setup(uint8_t* smem_raw, uint32_t ctl_offset, const Params& p) {
   const uint32_t raw = ptx::smem_u32(smem_raw);
   Layout L;
+  L.heads4d = p.bshd ? p.heads : 0;
   L.base = (raw + 1023u) & ~1023u;
   L.ctl = reinterpret_cast<SmemCtl*>(smem_raw + (L.base - raw) + ctl_offset);
   return L;
@@ -232,8 +261,8 @@ __device__ __forceinline__ void stream_tiles(const Layout& L, const Sync& s, con
   if (s.lane == 0) {
     const uint32_t fb = s.bar(ctl->fixed_full);
     ptx::mbar_arrive_expect_tx(fb, 2 * kTileBytes);
-    load_tile(L.fixed(0), f0, fb, frow, bh);
-    load_tile(L.fixed(1), f1, fb, frow, bh);
+    load_tile(L.fixed(0), f0, fb, frow, bh, L.heads4d);
+    load_tile(L.fixed(1), f1, fb, frow, bh, L.heads4d);
   }
   __syncwarp();
   int slot = 0;
@@ -244,7 +273,7 @@ __device__ __forceinline__ void stream_tiles(const Layout& L, const Sync& s, con
     if (s.lane == 0) {
       const uint32_t fb = s.bar(ctl->ring_full[slot]);
       ptx::mbar_arrive_expect_tx(fb, kTileBytes);
-      load_tile(L.ring(slot), (t & 1) ? r1 : r0, fb, (t0 + (t >> 1)) * kBlockM, bh);
+      load_tile(L.ring(slot), (t & 1) ? r1 : r0, fb, (t0 + (t >> 1)) * kBlockM, bh, L.heads4d);
     }
     __syncwarp();
     used |= 1u << slot;
@@ -284,8 +313,8 @@ __device__ __forceinline__ void dq_loads(const Layout& L, const Sync& s, const C
   if (s.lane == 0) {
     const uint32_t fb = s.bar(ctl->fixed_full);
     ptx::mbar_arrive_expect_tx(fb, 2 * kTileBytes);
-    load_tile(L.fixed(0), tm_q, fb, qrow, bh);
-    load_tile(L.fixed(1), tm_do, fb, qrow, bh);
+    load_tile(L.fixed(0), tm_q, fb, qrow, bh, L.heads4d);
+    load_tile(L.fixed(1), tm_do, fb, qrow, bh, L.heads4d);
   }
   __syncwarp();
   int ks = 0, vs = 0;
@@ -296,7 +325,7 @@ __device__ __forceinline__ void dq_loads(const Layout& L, const Sync& s, const C
     if (s.lane == 0) {
       const uint32_t fb = s.bar(ctl->ring_full[slot]);
       ptx::mbar_arrive_expect_tx(fb, kTileBytes);
-      load_tile(L.ring(slot), tm, fb, row, bh);
+      load_tile(L.ring(slot), tm, fb, row, bh, L.heads4d);
     }
     __syncwarp();
     used |= 1u << slot;
@@ -325,7 +354,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (threadIdx.x == 0) atomicOr(&g_attn_status, kStatusSmemAlign);
     return;
   }
-  const Layout L = setup(smem_raw, kCtlOffsetDq);
+  const Layout L = setup(smem_raw, kCtlOffsetDq, p);
   SmemCtl* ctl = L.ctl;
   const uint32_t warp = threadIdx.x >> 5;
   Sync s{ctl, threadIdx.x & 31u};
@@ -463,7 +492,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
     if (ok && s.wait(ctl->acc_full, 0, kStatusTimeoutSoftmax)) {
       ptx::tc_fence_after();
-      uint8_t* out = static_cast<uint8_t*>(p.out0) + gi * (kHeadDim * 2);
+      uint8_t* out = static_cast<uint8_t*>(p.out0) + row_offset(p, bh, qrow, p.sq);
 #pragma unroll 2
       for (int c = 0; c < 8; ++c) {
         uint32_t acc[16];
@@ -506,7 +535,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  const Layout L = setup(smem_raw, kCtlOffsetDkdv);
+  const Layout L = setup(smem_raw, kCtlOffsetDkdv, p);
   SmemCtl* ctl = L.ctl;
   const uint32_t warp = threadIdx.x >> 5;
   Sync s{ctl, threadIdx.x & 31u};
@@ -683,7 +712,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       }
     }
     const bool row_ok = krow < p.sk;
-    const size_t gk = (static_cast<size_t>(bh) * p.sk + krow) * (kHeadDim * 2);
+    const size_t gk = row_offset(p, bh, krow, p.sk);
     uint8_t* dk = static_cast<uint8_t*>(p.out0) + gk;
     uint8_t* dv = static_cast<uint8_t*>(p.out1) + gk;
     if (nq == 0) {

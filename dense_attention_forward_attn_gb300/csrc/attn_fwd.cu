@@ -432,7 +432,6 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
                         float* delta, int B, int H, int Sq, int Sk, int D, float scale, int flags,
                         void* stream) {
   if (flags & ~ATTN_FLAGS_ALL) return ATTN_ERR_INVALID_ARG;
-  if (flags & ATTN_FLAG_BSHD) return ATTN_ERR_UNSUPPORTED;
   int rc = check_shape(B, H, Sq, Sk, D);
   if (rc != ATTN_OK) return rc;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -481,11 +480,12 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   rc = device_info(dev, &info);
   if (rc != ATTN_OK) return rc;
 
+  const bool bshd = (flags & ATTN_FLAG_BSHD) != 0;
   alignas(64) CUtensorMap tm_q, tm_k, tm_v, tm_do;
-  if (encode_qkv(&tm_q, q, B, H, Sq, false) != ATTN_OK ||
-      encode_qkv(&tm_k, k, B, H, Sk, false) != ATTN_OK ||
-      encode_qkv(&tm_v, v, B, H, Sk, false) != ATTN_OK ||
-      encode_qkv(&tm_do, dout, B, H, Sq, false) != ATTN_OK)
+  if (encode_qkv(&tm_q, q, B, H, Sq, bshd) != ATTN_OK ||
+      encode_qkv(&tm_k, k, B, H, Sk, bshd) != ATTN_OK ||
+      encode_qkv(&tm_v, v, B, H, Sk, bshd) != ATTN_OK ||
+      encode_qkv(&tm_do, dout, B, H, Sq, bshd) != ATTN_OK)
     return ATTN_ERR_CUDA;
 
   attn::bwd::Params p;
@@ -498,6 +498,8 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   p.q_valid_last = Sq - (p.q_tiles - 1) * attn::kBlockM;
   p.kv_valid_last = Sk - (p.kv_tiles - 1) * attn::kBlockN;
   p.bh = static_cast<int>(bh);
+  p.heads = H;
+  p.bshd = bshd ? 1 : 0;
   p.causal = (flags & ATTN_FLAG_CAUSAL) ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
@@ -505,7 +507,8 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
 
   const int64_t rows = bh * Sq;
   attn::bwd::attn_bwd_delta_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
-      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), delta, rows);
+      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), delta, rows, H, Sq,
+      p.bshd);
   p.out0 = dk;
   p.out1 = dv;
   attn::bwd::attn_bwd_dkdv_kernel<<<static_cast<unsigned>(bh * p.kv_tiles), attn::bwd::kThreads,

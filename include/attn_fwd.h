@@ -155,13 +155,14 @@ int attn_fwd_host_chunking(int B, int H, int Sq, int Sk, int flags, int num_sms,
  * Line by Line", the exp2 question: natural-log units, or the gradients are
  * wrong while the forward is right).
  *
- *   q, o, dout, dq   device, BF16, [B, H, Sq, D] contiguous (dq written)
- *   k, v, dk, dv     device, BF16, [B, H, Sk, D] contiguous (dk, dv written)
- *   lse              device, fp32, [B, H, Sq], read (attn_fwd's lse)
+ *   q, o, dout, dq   device, BF16, [B, H, Sq, D] contiguous (dq written), or
+ *                    [B, Sq, H, D] with ATTN_FLAG_BSHD
+ *   k, v, dk, dv     device, BF16, [B, H, Sk, D] contiguous (dk, dv written), or
+ *                    [B, Sk, H, D] with ATTN_FLAG_BSHD
+ *   lse              device, fp32, [B, H, Sq], read (attn_fwd's lse), either layout
  *   delta            device, fp32, [B, H, Sq]: scratch owned by the caller, written
  *                    with delta_i and read back by the same call
- *   flags            0 or ATTN_FLAG_CAUSAL (must match the forward); ATTN_FLAG_BSHD
- *                    gives ATTN_ERR_UNSUPPORTED
+ *   flags            ATTN_FLAG_CAUSAL (must match the forward) and/or ATTN_FLAG_BSHD
  *
  * Sizes, scale, alignment (16 bytes for BF16 tensors, 4 for lse and delta),
  * ownership and error rules as attn_fwd; no output may overlap any input or
