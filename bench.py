@@ -42,6 +42,10 @@ METRIC = "attention fwd TFLOPS (4·B·H·S²·D) at S=4K/8K/16K, % of GB300 BF16
 UNIT = "TFLOP/s"
 WORKLOAD = "S=4K/8K/16K sweep (B=4/2/1, H=16, D=128, BF16, non-causal)"
 FALLBACK_BF16_TFLOPS = 1900.0
+# MUFU exp2 rate per SM: 4 sub-partitions x one 32-lane ex2 warp instruction per 4 clocks, as
+# measured on GB300 with back-to-back ex2.approx.ftz; the co-roofline's peak is this x SMs x the
+# SM clock sampled during the timed region.
+MUFU_EX2_PER_CLK_PER_SM = 32
 
 # --row: (metric, workload, FLOP factor on 4*B*H*S^2*D)
 ROWS = {
@@ -315,25 +319,33 @@ def run_ours(args):
         ms = [kev[s][i][0].elapsed_time(kev[s][i][1]) for s in range(args.steps)]
         avg = sum(ms) / len(ms)
         kernel_ms_total += avg
+        p10, p50, p90 = (float(np.percentile(ms, x)) for x in (10, 50, 90))
+        # minimum HBM bytes of the forward: Q, K, V read once, O and LSE written once
+        hbm = 2 * (2 * w.B * w.H * w.Sq * w.D + 2 * w.B * w.H * w.Sk * w.D) + 4 * w.B * w.H * w.Sq
         per_cfg[w.name] = {"ms_avg": round(avg, 4), "ms_min": round(min(ms), 4),
-                           "tflops": round(flop_factor * w.flops / (avg * 1e-3) / 1e12, 1)}
+                           "ms_p10": round(p10, 4), "ms_p50": round(p50, 4), "ms_p90": round(p90, 4),
+                           "tflops": round(flop_factor * w.flops / (avg * 1e-3) / 1e12, 1),
+                           "tflops_p50": round(flop_factor * w.flops / (p50 * 1e-3) / 1e12, 1)}
+        if not backward:
+            per_cfg[w.name]["hbm_min_gbs"] = round(hbm / (avg * 1e-3) / 1e9, 1)
     status = attn.device_status()
 
-    # ---------------- end to end with host buffers (forward rows): attn.fwd on pinned CPU tensors
-    # runs attn_fwd_host, the C-ABI entry point that copies in chunks overlapped with the kernel
+    # ---------------- end to end with host buffers (forward rows): attn.fwd_host_batch on pinned
+    # CPU tensors runs attn_fwd_host (the C-ABI entry point that copies in chunks overlapped with
+    # the kernels) for the step's three shapes, each on its own stream, and returns their results
     e2e = None
     if not backward:
         h2d = sum(sum(t.numel() * t.element_size() for t in host) for _, _, host, *_ in shapes)
         d2h = sum(o.numel() * o.element_size() + lse.numel() * 4 for *_, o, lse, _x in shapes)
         e2e_steps = max(2, min(args.steps, 10))
-        for w, _, host, *_ in shapes:   # warm the pinned output buffers
-            attn.fwd(host[0], host[1], host[2], scale=w.scale, causal=causal, layout=layout)
+        problems = [dict(q=host[0], k=host[1], v=host[2], scale=w.scale, causal=causal, layout=layout)
+                    for w, _, host, *_ in shapes]
+        for _ in range(max(3, args.warmup)):   # warm-up: pinned output buffers, side streams
+            results = attn.fwd_host_batch(problems)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
-            for w, _, host, *_ in shapes:
-                o_h, lse_h = attn.fwd(host[0], host[1], host[2], scale=w.scale, causal=causal,
-                                      layout=layout)
+            results = attn.fwd_host_batch(problems)   # the step's three shapes, one call
         torch.cuda.synchronize()
         e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
         e2e = {"value": round(ws * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
@@ -351,6 +363,16 @@ def run_ours(args):
     tr = [_traffic_for(w.name) for w, *_ in shapes]
     if row == "dense" and all(t is not None for t in tr):
         traffic = sum(tr) / len(tr)
+    # co-roofline: one exp2 per score through the MUFU unit
+    co = None
+    if not backward and clk.get("sm_mhz"):
+        exps = sum(w.B * w.H * w.Sq * w.Sk * (0.5 if causal else 1.0) for w, *_ in shapes)
+        ex_rate = exps / (kernel_ms_total * 1e-3)
+        ex_peak = MUFU_EX2_PER_CLK_PER_SM * torch.cuda.get_device_properties(dev).multi_processor_count \
+            * clk["sm_mhz"] * 1e6
+        co = {"bound": "mufu", "achieved": round(ex_rate / 1e12, 3), "peak": round(ex_peak / 1e12, 3),
+              "unit": "Texp2/s", "frac": round(ex_rate / ex_peak, 4),
+              "peak_kind": "derived: 32 ex2/clk/SM (measured) x SMs x sampled SM clock"}
     cpu = None
     if ws == 1 and not args.no_cpu_baseline and row == "dense":
         v, cores, sample, _t = oracle_sample_tflops([(w, bits) for w, bits, *_ in shapes], 12.0)
@@ -368,6 +390,7 @@ def run_ours(args):
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                      "unit": UNIT, "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_kind": f"{peak_kind} burst bf16 (cuBLAS)"},
+        "co_roofline": co,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps * len(shapes) * (3 if backward else 1),

@@ -222,8 +222,49 @@ def fwd(q, k, v, scale: float | None = None, return_lse: bool = True, causal: bo
     return o, lse
 
 
+_side_streams = {}
+
+
+def fwd_host_batch(problems):
+    """Several host-buffer forwards at once: each problem is a dict with q, k, v (CPU BF16) and
+    optional scale, causal, layout, return_lse.  Each goes through attn_fwd_host on its own side
+    stream (after the work already on the current stream), so one problem's copies overlap the
+    others' kernels; returns [(o, lse)] (pinned CPU tensors) once all are complete."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device())
+    cur = torch.cuda.current_stream(dev)
+    streams = _side_streams.setdefault(dev.index, [])
+    while len(streams) < len(problems):
+        streams.append(torch.cuda.Stream(dev))
+    pending = []
+    for pb, st in zip(problems, streams):
+        st.wait_stream(cur)
+        with torch.cuda.stream(st):
+            pending.append(_fwd_host_enqueue(pb["q"], pb["k"], pb["v"], pb.get("scale"),
+                                             pb.get("return_lse", True), pb.get("causal", False),
+                                             pb.get("layout", "bhsd")))
+    for st in streams[:len(problems)]:
+        cur.wait_stream(st)
+    cur.synchronize()
+    return [(o, lse) for o, lse, _keep in pending]
+
+
 def _fwd_host(q, k, v, B, H, Sq, Sk, D, scale, return_lse, causal, layout):
     import torch
+    o, lse, keep = _fwd_host_enqueue(q, k, v, scale, return_lse, causal, layout)
+    torch.cuda.current_stream().synchronize()
+    del keep
+    return o, lse
+
+
+def _fwd_host_enqueue(q, k, v, scale, return_lse, causal, layout):
+    """Enqueue attn_fwd_host on the current stream; returns (o, lse, keep) -- keep (the device
+    workspace and the pinned inputs) must stay referenced until the stream has finished the
+    call, since the library's copies are not tracked by PyTorch's allocators."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n)
+    B, H, Sq, Sk, D = _dims(q, k, layout)
     if k.is_cuda or v.is_cuda:
         raise ValueError("q, k, v must all be CPU tensors or all CUDA tensors")
     kv_shape = (B, Sk, H, D) if layout == "bshd" else (B, H, Sk, D)
@@ -248,8 +289,7 @@ def _fwd_host(q, k, v, B, H, Sq, Sk, D, scale, return_lse, causal, layout):
                            float(scale), flags, work.data_ptr(), ws.value, stream.cuda_stream)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_host")
-    stream.synchronize()
-    return o, lse
+    return o, lse, (work, q, k, v)
 
 
 def bwd(q, k, v, o, dout, lse, scale: float | None = None, causal: bool = False,

@@ -371,3 +371,23 @@ def test_host_buffer_forward_full_size():
     o64 = o_h.float().numpy().astype(np.float64).reshape(-1, w.Sq, w.D)
     _assert_close(o64[bh, rows], o_ref, lse_h.numpy().astype(np.float64).reshape(-1, w.Sq)[bh, rows],
                   lse_ref)
+
+
+def test_host_buffer_batch_matches_single_calls():
+    """fwd_host_batch: several host-buffer problems in flight at once (own streams, shared copy
+    streams of the library); each result bitwise equal to its own device-path call."""
+    specs = [((2, 40, 1024, 1024), False, "bhsd"), ((3, 5, 300, 700), True, "bhsd"),
+             ((9, 3, 640, 640), False, "bshd")]
+    problems, expect = [], []
+    for i, ((B, H, Sq, Sk), causal, layout) in enumerate(specs):
+        tens = [wl.bits_to_torch(x) for x in wl.make_inputs_bits(B, H, Sq, Sk, 128, seed=50 + i)]
+        if layout == "bshd":
+            tens = [t.transpose(1, 2).contiguous() for t in tens]
+        problems.append(dict(q=tens[0], k=tens[1], v=tens[2], scale=0.09, causal=causal, layout=layout))
+        o_d, lse_d = attn.fwd(*(t.cuda() for t in tens), scale=0.09, causal=causal, layout=layout)
+        expect.append((o_d.cpu(), lse_d.cpu()))
+    for rep in range(2):
+        got = attn.fwd_host_batch(problems)
+        for (o, lse), (o_e, lse_e) in zip(got, expect):
+            assert torch.equal(o, o_e) and torch.equal(lse, lse_e)
+    assert attn.device_status() == 0
