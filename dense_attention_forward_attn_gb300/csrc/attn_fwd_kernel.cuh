@@ -11,8 +11,11 @@
 //   * Chapter 3: Q/K/V are staged by TMA with 128-byte swizzle; Q and K are
 //     K-major operands, V is the MN-major B operand of P*V.
 //   * Chapter 4 / 5 / 12: warp roles -- two softmax warpgroups (one per Q tile),
-//     one correction warpgroup (conditional O rescale and the epilogue), one TMA
-//     warp and one MMA-issuing warp; handoffs use mbarriers only.
+//     one correction warpgroup (conditional O rescale), one TMA warp and one
+//     MMA-issuing warp; handoffs use mbarriers only.  Unlike the pages, each
+//     softmax warpgroup also runs its own Q tile's epilogue, before the next
+//     item's first P (so O's columns are free once that P is published): O is
+//     read out of TMEM and O and LSE are stored from registers.
 //   * Chapter 6: a ring of KV_STAGES shared slots, each holding one K or one V
 //     tile; token t and t+KV_STAGES share a slot; a K token is released after
 //     the last Q tile's Q*K^T, a V token after the last Q tile's P*V.
@@ -108,16 +111,11 @@ struct alignas(8) SmemCtl {
   uint64_t s_full[2];      // MMA -> softmax: S_q(i) in TMEM
   uint64_t p_full[2];      // softmax (P in TMEM) + correction (O rescaled or untouched) -> MMA
   uint64_t stats_full[2];  // softmax -> correction: per-row rescale factor published
-  uint64_t o_full[2];      // MMA -> correction: last P*V of the item done
-  // softmax -> correction: final row max / row sum of an item published, one barrier per item
-  // parity: the softmax may publish item r+1 before the correction has read item r.
-  uint64_t final_full[2][2];   // [stage][item parity]
+  uint64_t o_full[2];      // MMA -> softmax: last P*V of the item done (O final in TMEM)
   uint64_t drain;
   uint32_t tmem_base;
   volatile int abort_flag;
   float alpha[2][2][kBlockM];   // [stage][tile parity][row]
-  float row_m[2][2][kBlockM];   // [stage][item parity][row], base-2 units
-  float row_l[2][2][kBlockM];   // [stage][item parity][row]
 };
 
 constexpr uint32_t kCtlOffset = (2 + kKvStages) * kTileBytes;
@@ -571,6 +569,45 @@ __device__ __forceinline__ float row_max_128(const uint32_t (&sr)[4][32]) {
   return fmaxf(ptx::fmax3(d[0], d[1], d[2]), fmaxf(d[3], d[4]));
 }
 
+// Item epilogue of stage q, run by the stage's own softmax warpgroup: O_q (final once the item's
+// last P*V is done, o_full) is read from TMEM, scaled by 1/l and packed to BF16 in registers;
+// once read, O_q's columns are free for the next item's first P*V, which waits for the next
+// P this warpgroup publishes.  The stores to global memory follow from the registers.
+__device__ __forceinline__ bool epilogue_read(const Ctx& c, int q, uint32_t o_parity, float inv_l,
+                                              uint32_t (&pk)[64]) {
+  if (!c.wait(c.ctl->o_full[q], o_parity, kStatusTimeoutSoftmax)) return false;
+  ptx::tc_fence_after();
+  const uint32_t taddr_o = c.tmem + ((32u * (c.warp & 3u)) << 16) + col_o(q);
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    uint32_t r[32];
+    ptx::tmem_ld_32x32b_x32(taddr_o + 32 * cc, r);
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[16 * cc + i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l,
+                                         __uint_as_float(r[2 * i + 1]) * inv_l);
+  }
+  ptx::tc_fence_before();
+  return true;
+}
+
+// O row and LSE of this thread's query row of stage q of item w (rows past a ragged end of Q
+// are computed but not stored).  LSE = (kept max + log2 l) * ln 2.
+__device__ __forceinline__ void epilogue_store(const Params& p, int q, const WorkItem& w, int row,
+                                               float m, float l, const uint32_t (&pk)[64]) {
+  const int grow = (w.qt0 + q) * kBlockM + row;
+  if (grow >= p.sq) return;
+  const int b = w.bh / p.heads, h = w.bh - b * p.heads;
+  uint8_t* out = static_cast<uint8_t*>(p.o) +
+                 (b * p.o_batch_stride + h * p.o_head_stride + grow * p.o_row_stride) * 2;
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    ptx::st_global_v4(out + 16 * i, pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+  if (p.lse != nullptr)
+    p.lse[static_cast<size_t>(w.bh) * p.sq + grow] = (m + log2f(l)) * 0.69314718055994530942f;
+}
+
 __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int q) {
   SmemCtl* ctl = c.ctl;
   const uint32_t row_base = 32u * (c.warp & 3u);
@@ -582,7 +619,10 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
   const float scale_log2 = zero_scale ? 1.f : p.scale_log2;
   const uint32_t keep = zero_scale ? 0u : 0xffffffffu;
   uint32_t tphase = 0;
-  uint32_t items_q = 0;
+  uint32_t o_parity = 0;     // o_full phase of the previous item
+  bool have_prev = false;    // an item whose epilogue is still to do
+  WorkItem wp;
+  float m_prev = 0.f, l_prev = 1.f;
 
   for (int r = 0;; ++r) {
     const int item = item_of(r, blockIdx.x, gridDim.x, p.num_items, p.causal != 0);
@@ -591,6 +631,15 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
     const int ntiles = w.n[q];
     if (ntiles == 0) continue;
     const int qtile = w.qt0 + q;
+    // The previous item's epilogue, before this item's first P: its O columns are then free
+    // when that P is published (the first P*V of an item overwrites O), and the read overlaps
+    // this item's first Q*K^T, issued right after the previous item's last P*V.
+    if (have_prev) {
+      uint32_t pk[64];
+      if (!epilogue_read(c, q, o_parity, 1.0f / l_prev, pk)) return;
+      epilogue_store(p, q, wp, row, m_prev, l_prev, pk);
+      o_parity ^= 1u;
+    }
     float m_kept = 0.f;   // base-2 units; set on the first tile
     float l = 0.f;
     for (int j = 0; j < ntiles; ++j) {
@@ -626,59 +675,26 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
       l += produce_p(c, q, sr, scale_log2, m_kept, taddr_s);
       tphase ^= 1u;
     }
-    ctl->row_m[q][items_q & 1u][row] = m_kept;
-    ctl->row_l[q][items_q & 1u][row] = l;
-    c.arrive(ctl->final_full[q][items_q & 1u]);
-    ++items_q;
+    have_prev = true;
+    wp = w;
+    m_prev = m_kept;
+    l_prev = l;
+  }
+  if (have_prev) {
+    uint32_t pk[64];
+    if (!epilogue_read(c, q, o_parity, 1.0f / l_prev, pk)) return;
+    epilogue_store(p, q, wp, row, m_prev, l_prev, pk);
   }
 }
 
 // ------------------------------------------------------------------ correction warpgroup
-__device__ __forceinline__ bool epilogue(const Ctx& c, const Params& p, int q, const WorkItem& w,
-                                         uint32_t idx) {
-  SmemCtl* ctl = c.ctl;
-  if (!c.wait(ctl->final_full[q][idx & 1u], (idx >> 1) & 1u, kStatusTimeoutCorrection)) return false;
-  if (!c.wait(ctl->o_full[q], idx & 1u, kStatusTimeoutCorrection)) return false;
-  ptx::tc_fence_after();
-  const uint32_t row_base = 32u * (c.warp & 3u);
-  const int row = static_cast<int>(row_base + c.lane);
-  const float m = ctl->row_m[q][idx & 1u][row];
-  const float l = ctl->row_l[q][idx & 1u][row];
-  const float inv_l = 1.0f / l;
-  const int grow = (w.qt0 + q) * kBlockM + row;
-  const bool store = grow < p.sq;   // rows past a ragged end of Q are computed but not stored
-  const int b = w.bh / p.heads, h = w.bh - b * p.heads;
-  uint8_t* out = static_cast<uint8_t*>(p.o) +
-                 (b * p.o_batch_stride + h * p.o_head_stride + grow * p.o_row_stride) * 2;
-  const uint32_t taddr_o = c.tmem + (row_base << 16) + col_o(q);
-#pragma unroll 2
-  for (int cc = 0; cc < 8; ++cc) {
-    uint32_t r[16];
-    ptx::tmem_ld_32x32b_x16(taddr_o + 16 * cc, r);
-    ptx::tmem_wait_ld();
-    uint32_t pk[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
-    if (store) {
-      ptx::st_global_v4(out + cc * 32, pk[0], pk[1], pk[2], pk[3]);
-      ptx::st_global_v4(out + cc * 32 + 16, pk[4], pk[5], pk[6], pk[7]);
-    }
-  }
-  if (p.lse != nullptr && store)
-    p.lse[static_cast<size_t>(w.bh) * p.sq + grow] = (m + log2f(l)) * 0.69314718055994530942f;
-  ptx::tc_fence_before();
-  return true;
-}
-
+// Per KV tile and stage: if any row of the warp rebased its max, O_q *= alpha in TMEM; then O_q
+// is safe for the next P*V (p_full, together with the softmax's P).
 __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
   SmemCtl* ctl = c.ctl;
   const uint32_t row_base = 32u * (c.warp & 3u);
   const int row = static_cast<int>(row_base + c.lane);
   uint32_t tphase[2] = {0, 0};
-  uint32_t items_done[2] = {0, 0};
-  bool pending[2] = {false, false};
-  WorkItem pend_w[2];
 
   for (int r = 0;; ++r) {
     const int item = item_of(r, blockIdx.x, gridDim.x, p.num_items, p.causal != 0);
@@ -689,12 +705,9 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         if (j >= w.n[q]) continue;
-        if (j == 0 && pending[q]) {
-          if (!epilogue(c, p, q, pend_w[q], items_done[q])) return;
-          ++items_done[q];
-          pending[q] = false;
-        }
         if (!c.wait(ctl->stats_full[q], tphase[q], kStatusTimeoutCorrection)) return;
+        // alpha is 1 on an item's first tile, so the previous item's O, which its softmax
+        // warpgroup may still be reading, is not touched here.
         const float a = ctl->alpha[q][tphase[q]][row];
         if (__any_sync(0xffffffffu, a != 1.0f)) {
           const uint32_t taddr_o = c.tmem + (row_base << 16) + col_o(q);
@@ -715,16 +728,7 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
         tphase[q] ^= 1u;
       }
     }
-    pending[0] = true;
-    pend_w[0] = w;
-    if (w.n[1] > 0) {
-      pending[1] = true;
-      pend_w[1] = w;
-    }
   }
-#pragma unroll
-  for (int q = 0; q < 2; ++q)
-    if (pending[q] && !epilogue(c, p, q, pend_w[q], items_done[q])) return;
 }
 
 // ------------------------------------------------------------------ kernel
@@ -749,8 +753,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ptx::mbar_init(c.bar(ctl->p_full[q]), 2 * kArrivePerWG);   // softmax + correction WGs
       ptx::mbar_init(c.bar(ctl->stats_full[q]), kArrivePerWG);
       ptx::mbar_init(c.bar(ctl->o_full[q]), 1);
-      ptx::mbar_init(c.bar(ctl->final_full[q][0]), kArrivePerWG);
-      ptx::mbar_init(c.bar(ctl->final_full[q][1]), kArrivePerWG);
     }
     for (int s = 0; s < kKvStages; ++s) {
       ptx::mbar_init(c.bar(ctl->kv_full[s]), 1);
