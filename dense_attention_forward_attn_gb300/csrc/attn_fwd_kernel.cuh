@@ -47,6 +47,9 @@
 #ifndef ATTN_KV_STAGES
 #define ATTN_KV_STAGES 3
 #endif
+#ifndef ATTN_L2_PREFETCH
+#define ATTN_L2_PREFETCH 2   // K/V tiles prefetched into L2 ahead of the ring's loads
+#endif
 // 1: one elected lane per warp arrives on the consumer barriers (counts per warp);
 // 0: every thread arrives (counts per thread).
 #ifndef ATTN_ARRIVE_PER_WARP
@@ -302,6 +305,19 @@ __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const C
       ptx::tma_load_3d(dst, tm, fb, col, row, bh);
     }
   };
+  // L2 prefetch of a K or V tile ATTN_L2_PREFETCH tiles ahead of its load: the first CTA to
+  // read a tile of a head otherwise waits for DRAM, and so do the CTAs reading it with it.
+  auto prefetch = [&](const CUtensorMap* tm, int bh, int row) {
+    if (c.lane != 0) return;
+    if (p.bshd) {
+      const int b = bh / p.heads, h = bh - b * p.heads;
+      ptx::tma_prefetch_4d(tm, 0, h, row, b);
+      ptx::tma_prefetch_4d(tm, 64, h, row, b);
+    } else {
+      ptx::tma_prefetch_3d(tm, 0, row, bh);
+      ptx::tma_prefetch_3d(tm, 64, row, bh);
+    }
+  };
   auto load_kv = [&](const CUtensorMap* tm, int bh, int row) -> bool {
     if (!c.wait(ctl->kv_empty[slot], phase ^ 1u, kStatusTimeoutLoad)) return false;
     if (c.lane == 0) {
@@ -335,11 +351,24 @@ __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const C
     const WorkItem w = decode_item(item, p);
     const int row0 = w.qt0 * kBlockM;
     const int ntiles = w.n[1] > 0 ? w.n[1] : w.n[0];   // n[1] >= n[0] whenever it is non-zero
+#if ATTN_L2_PREFETCH > 0
+    for (int j = 0; j < ATTN_L2_PREFETCH && j < ntiles; ++j) {
+      prefetch(tm_k, w.bh, j * kBlockN);
+      prefetch(tm_v, w.bh, j * kBlockN);
+    }
+#endif
     ok = load_q(0, w.bh, row0) && load_kv(tm_k, w.bh, 0);
     if (ok && w.n[1] > 0) ok = load_q(1, w.bh, row0 + kBlockM);
     if (ok) ok = load_kv(tm_v, w.bh, 0);
-    for (int j = 1; ok && j < ntiles; ++j)
+    for (int j = 1; ok && j < ntiles; ++j) {
+#if ATTN_L2_PREFETCH > 0
+      if (j + ATTN_L2_PREFETCH - 1 < ntiles) {
+        prefetch(tm_k, w.bh, (j + ATTN_L2_PREFETCH - 1) * kBlockN);
+        prefetch(tm_v, w.bh, (j + ATTN_L2_PREFETCH - 1) * kBlockN);
+      }
+#endif
       ok = load_kv(tm_k, w.bh, j * kBlockN) && load_kv(tm_v, w.bh, j * kBlockN);
+    }
   }
   if (!ok) {
     // Stop issuing; wait for the copies this warp already started.
