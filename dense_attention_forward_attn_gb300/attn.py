@@ -25,6 +25,7 @@ ATTN_ERR_CUDA = -4
 ATTN_ERR_TOO_LARGE = -5
 ATTN_FLAG_CAUSAL = 1
 ATTN_FLAG_BSHD = 2
+ATTN_FLAG_TEST_WITHHOLD = 0x100   # test hook: see include/attn_fwd.h
 
 
 class AttnError(RuntimeError):

@@ -257,6 +257,7 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
   p.bh = static_cast<int>(bh);
   p.causal = (flags & ATTN_FLAG_CAUSAL) ? 1 : 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  p.test_withhold = (flags & ATTN_FLAG_TEST_WITHHOLD) ? 1 : 0;
   const int grid = p.num_items < info.num_sms ? p.num_items : info.num_sms;
 
   attn::attn_fwd_kernel<<<grid, attn::kThreads, attn::kSmemBytes,

@@ -141,6 +141,8 @@ struct Params {
   int bh;           // B * H
   int causal;       // query i attends keys j <= i (top-left aligned)
   float scale_log2; // scale * log2(e)
+  int test_withhold;  // test hook: CTA 0's TMA warp never loads its first K tile, so the MMA
+                      // warp's bounded wait on it expires (exercises the failure path)
 };
 
 struct WorkItem {
@@ -318,8 +320,14 @@ __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const C
       ptx::tma_prefetch_3d(tm, 64, row, bh);
     }
   };
+  bool withhold = p.test_withhold != 0 && blockIdx.x == 0;
   auto load_kv = [&](const CUtensorMap* tm, int bh, int row) -> bool {
     if (!c.wait(ctl->kv_empty[slot], phase ^ 1u, kStatusTimeoutLoad)) return false;
+    if (withhold) {   // the slot is skipped: nothing is loaded into it, nothing to drain
+      withhold = false;
+      if (++slot == kKvStages) { slot = 0; phase ^= 1u; }
+      return true;
+    }
     if (c.lane == 0) {
       const uint32_t fb = c.bar(ctl->kv_full[slot]);
       ptx::mbar_arrive_expect_tx(fb, kTileBytes);

@@ -77,7 +77,12 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 /* Flags of attn_fwd_ex. */
 #define ATTN_FLAG_CAUSAL 1 /* query i attends keys j <= i (top-left aligned, i and j from 0) */
 #define ATTN_FLAG_BSHD 2   /* q, k, v, o are [B, S, H, D] contiguous (lse stays [B, H, Sq]) */
-#define ATTN_FLAGS_ALL (ATTN_FLAG_CAUSAL | ATTN_FLAG_BSHD)
+/* Test hook, attn_fwd_ex only: in CTA 0 the TMA warp never loads its first K tile, so the MMA
+ * warp's bounded wait on it expires (2 s); the CTA then stops, records status bits (see
+ * attn_device_status) and exits, leaving its outputs unspecified.  For testing the failure path;
+ * other CTAs and later calls are unaffected. */
+#define ATTN_FLAG_TEST_WITHHOLD 0x100
+#define ATTN_FLAGS_ALL (ATTN_FLAG_CAUSAL | ATTN_FLAG_BSHD | ATTN_FLAG_TEST_WITHHOLD)
 
 /*
  * attn_fwd_ex -- attn_fwd with options.  Arguments, ownership, errors and
