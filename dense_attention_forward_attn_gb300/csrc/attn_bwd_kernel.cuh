@@ -65,6 +65,7 @@ struct alignas(8) SmemCtl {
   // dQ kernel: S of KV tile j in TMEM buffer j&1, one barrier per buffer (the product for tile j+2
   // may complete before the elementwise warps waited for tile j+1).
   uint64_t sb_full[2];
+  uint64_t epi_full;            // dK/dV kernel: the elementwise warps staged dK, dV in SMEM
   uint64_t vec_sync;            // elementwise warps exchanged per-column vectors (dK/dV)
   uint64_t drain;
   uint32_t tmem_base;
@@ -247,6 +248,7 @@ __device__ __forceinline__ void init_barriers(SmemCtl* ctl, const Sync& s) {
   ptx::mbar_init(s.bar(ctl->sb_full[0]), 1);
   ptx::mbar_init(s.bar(ctl->sb_full[1]), 1);
   ptx::mbar_init(s.bar(ctl->vec_sync), 4);
+  ptx::mbar_init(s.bar(ctl->epi_full), 4);
   ptx::mbar_init(s.bar(ctl->drain), 1);
   ctl->abort_flag = 0;
   ptx::fence_mbar_init();
@@ -533,6 +535,7 @@ __device__ __forceinline__ void dkdv_item(const Params& p, int& bh, int& kt, int
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                      const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const Layout L = setup(smem_raw, kCtlOffsetDkdv, p);
@@ -722,16 +725,52 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         zero_row(dv);
       }
     } else if (ok && s.wait(ctl->acc_full, 0, kStatusTimeoutSoftmax)) {
+      // Every product is done, so the Q/dO ring is free: dK (ring slot 0) and dV (slot 1) are
+      // staged there as BF16 in the TMA layout (two 64-column slabs, 128-byte swizzle) and stored
+      // with four tensor copies (rows past Sk are clipped by the tensor maps).
       ptx::tc_fence_after();
+      const uint32_t swz = static_cast<uint32_t>(r) & 7u;
 #pragma unroll 2
       for (int c = 0; c < 8; ++c) {
-        uint32_t acc[16];
-        ptx::tmem_ld_32x32b_x16(kTmemBase + lane_off + kColDK + 16 * c, acc);
-        ptx::tmem_wait_ld();
-        if (row_ok) store_cols16(dk + 32 * c, acc, p.scale);
-        ptx::tmem_ld_32x32b_x16(kTmemBase + lane_off + kColDV + 16 * c, acc);
-        ptx::tmem_wait_ld();
-        if (row_ok) store_cols16(dv + 32 * c, acc, 1.0f);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          uint32_t acc[16];
+          ptx::tmem_ld_32x32b_x16(kTmemBase + lane_off + (t ? kColDV : kColDK) + 16 * c, acc);
+          ptx::tmem_wait_ld();
+          const float mul = t ? 1.0f : p.scale;
+          uint32_t pk[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            pk[i] = ptx::pack_bf16x2(__uint_as_float(acc[2 * i]) * mul,
+                                     __uint_as_float(acc[2 * i + 1]) * mul);
+          const uint32_t line = L.ring(t) + (c >> 2) * kSlabBytes + static_cast<uint32_t>(r) * 128u;
+          const uint32_t u = 2u * (c & 3);
+          ptx::st_shared_v4(line + ((u ^ swz) << 4), pk[0], pk[1], pk[2], pk[3]);
+          ptx::st_shared_v4(line + (((u + 1u) ^ swz) << 4), pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      s.arrive(ctl->epi_full);
+      if (warp == 0) {
+        const bool staged = s.wait(ctl->epi_full, 0, kStatusTimeoutSoftmax);
+        if (staged && s.lane == 0) {
+          const int row0 = kt * kBlockN;
+          for (int t = 0; t < 2; ++t) {
+            const CUtensorMap* tm = t ? &tm_dv : &tm_dk;
+            for (int sl = 0; sl < 2; ++sl) {
+              const uint32_t src = L.ring(t) + sl * kSlabBytes;
+              if (L.heads4d) {
+                const int b = bh / L.heads4d, h = bh - b * L.heads4d;
+                ptx::tma_store_4d(tm, src, 64 * sl, h, row0, b);
+              } else {
+                ptx::tma_store_3d(tm, src, 64 * sl, row0, bh);
+              }
+            }
+          }
+          ptx::bulk_commit_group();
+          ptx::bulk_wait_all();
+        }
+        __syncwarp();
       }
     }
   }

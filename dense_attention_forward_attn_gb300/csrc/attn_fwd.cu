@@ -482,11 +482,13 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   if (rc != ATTN_OK) return rc;
 
   const bool bshd = (flags & ATTN_FLAG_BSHD) != 0;
-  alignas(64) CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  alignas(64) CUtensorMap tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv;
   if (encode_qkv(&tm_q, q, B, H, Sq, bshd) != ATTN_OK ||
       encode_qkv(&tm_k, k, B, H, Sk, bshd) != ATTN_OK ||
       encode_qkv(&tm_v, v, B, H, Sk, bshd) != ATTN_OK ||
-      encode_qkv(&tm_do, dout, B, H, Sq, bshd) != ATTN_OK)
+      encode_qkv(&tm_do, dout, B, H, Sq, bshd) != ATTN_OK ||
+      encode_qkv(&tm_dk, dk, B, H, Sk, bshd) != ATTN_OK ||
+      encode_qkv(&tm_dv, dv, B, H, Sk, bshd) != ATTN_OK)
     return ATTN_ERR_CUDA;
 
   attn::bwd::Params p;
@@ -513,7 +515,8 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   p.out0 = dk;
   p.out1 = dv;
   attn::bwd::attn_bwd_dkdv_kernel<<<static_cast<unsigned>(bh * p.kv_tiles), attn::bwd::kThreads,
-                                    attn::bwd::kSmemBytesDkdv, st>>>(tm_q, tm_k, tm_v, tm_do, p);
+                                    attn::bwd::kSmemBytesDkdv, st>>>(tm_q, tm_k, tm_v, tm_do,
+                                                                      tm_dk, tm_dv, p);
   p.out0 = dq;
   p.out1 = nullptr;
   attn::bwd::attn_bwd_dq_kernel<<<static_cast<unsigned>(bh * p.q_tiles), attn::bwd::kThreads,
