@@ -10,13 +10,15 @@
 //   attn_bwd_dkdv_kernel   one CTA per 128-row K/V tile: S^T = K Q^T and dP^T = V dO^T into
 //                          TMEM, P^T and dS^T (BF16) written back over their upper halves, then
 //                          dV += P^T dO and dK += dS^T Q with A from TMEM; loops over Q tiles
-//   attn_bwd_dq_kernel     one CTA per 128-row Q tile: S = Q K^T and dP = dO V^T, dS (BF16)
-//                          over S, dQ += dS K; loops over K/V tiles
+//   attn_bwd_dq_kernel     one CTA per pair of 128-row Q tiles: per tile S = Q K^T, then
+//                          dP = dO V^T over it, dS (BF16) over dP, dQ += dS K; loops over
+//                          K/V tiles, each feeding both tiles
 // Every gradient is written by exactly one CTA (no atomics: deterministic).  dQ repeats the
 // S and dP products of dK/dV (7 tile products per tile pair instead of 5).
 //
-// Roles per CTA (192 threads): warps 0-3 an elementwise warpgroup (one TMEM lane = one row per
-// thread), warp 4 TMA, warp 5 tcgen05.mma issue and TMEM allocation.  Tiles are staged by TMA
+// Roles: dK/dV CTA (192 threads): warps 0-3 an elementwise warpgroup (one TMEM lane = one row
+// per thread), warp 4 TMA, warp 5 tcgen05.mma issue and TMEM allocation; dQ CTA (384 threads):
+// one elementwise warpgroup per Q tile, then a TMA and an MMA warp.  Tiles are staged by TMA
 // with 128-byte swizzle exactly as in the forward kernel; every mbarrier wait is bounded.
 #pragma once
 #include <cuda.h>
@@ -31,11 +33,10 @@ constexpr int kThreads = 192;
 constexpr int kLoadWarp = 4;
 constexpr int kMmaWarp = 5;
 // Streamed tiles in flight.  dK/dV kernel: one ring of 4 slots (Q_i, dO_i alternate).  dQ kernel:
-// a K ring of 3 slots (ring slots 0..2: K_j lives from S_j to dQ += dS_j K_j) and a V ring of 2
-// (slots 3..4: V_j only feeds dP_j), so each tile is prefetched two products ahead.
-constexpr int kRing = 5;
+// two K slots and one V slot (K_j lives from S_j to the last dQ += dS_j K_j, V_j only feeds the
+// dP_j products).
+constexpr int kRing = 4;
 constexpr int kDkdvRing = 4;
-constexpr int kDqKRing = 3, kDqVRing = 2;
 
 struct Params {
   const void* lse;     // fp32 [B,H,Sq], natural log (the forward's output)
@@ -56,34 +57,27 @@ struct Params {
 struct alignas(8) SmemCtl {
   uint64_t fixed_full;          // the CTA's own two resident tiles are in SMEM
   uint64_t ring_full[kRing], ring_empty[kRing];
-  uint64_t mma_full;            // MMA -> elementwise: the two score-like tiles are in TMEM
-  uint64_t ew_full;             // elementwise -> MMA: BF16 operands written into TMEM
   uint64_t acc_full;            // MMA -> elementwise: the accumulators are final
   // dK/dV kernel, per Q tile: S^T and dP^T in TMEM (MMA -> elementwise), P^T and dS^T written
   // back (elementwise -> MMA).  Separate barriers let dV += P^T dO start before dS^T exists.
   uint64_t s_full, dp_full, p_ready, ds_ready;
-  // dQ kernel: S of KV tile j in TMEM buffer j&1, one barrier per buffer (the product for tile j+2
-  // may complete before the elementwise warps waited for tile j+1).
-  uint64_t sb_full[2];
   uint64_t epi_full;            // dK/dV kernel: the elementwise warps staged dK, dV in SMEM
+  // dQ kernel over a pair of Q tiles (a, b), per tile t: S_t in TMEM (dq_s_full), S_t read so
+  // dP_t may overwrite it (dq_x_read), dP_t in TMEM (dq_dp_full), dS_t written back
+  // (dq_ds_ready); dq_do_full: both dO tiles resident.
+  uint64_t dq_s_full[2], dq_x_read[2], dq_dp_full[2], dq_ds_ready[2], dq_do_full;
   uint64_t vec_sync;            // elementwise warps exchanged per-column vectors (dK/dV)
   uint64_t drain;
   uint32_t tmem_base;
   volatile int abort_flag;
-  float lse2[2][kBlockM];       // dK/dV kernel: LSE * log2(e) of the current Q tile's columns
+  float lse2[2][kBlockM];       // dK/dV kernel: -LSE * log2(e) of the current Q tile's columns
   float dlt[2][kBlockM];        // dK/dV kernel: delta of the current Q tile's columns
 };
 
 // dK/dV kernel: 2 resident + 4 ring tiles, control block, 1 KiB to align the base by hand.
 constexpr uint32_t kCtlOffsetDkdv = (2 + kDkdvRing) * kTileBytes;
 constexpr uint32_t kSmemBytesDkdv = kCtlOffsetDkdv + sizeof(SmemCtl) + 1024;
-// dQ kernel: 2 resident + 5 ring tiles and the control block fill the 227 KiB a CTA may have, with
-// no room to realign: the kernel requires the dynamic shared memory to start 1024-aligned (it
-// does when the kernel declares no static shared memory) and checks it.
-constexpr uint32_t kCtlOffsetDq = (2 + kRing) * kTileBytes;
-constexpr uint32_t kSmemBytesDq = kCtlOffsetDq + sizeof(SmemCtl);
 constexpr unsigned kStatusSmemAlign = 1u << 6;   // dynamic shared memory not 1024-aligned
-static_assert(kSmemBytesDq <= 227 * 1024, "dQ kernel shared memory exceeds a CTA's 227 KiB");
 
 // Bounded waits, as in the forward kernel: all 32 lanes call; false = timed out or aborted.
 struct Sync {
@@ -238,17 +232,20 @@ __device__ __forceinline__ void init_barriers(SmemCtl* ctl, const Sync& s) {
     ptx::mbar_init(s.bar(ctl->ring_full[i]), 1);
     ptx::mbar_init(s.bar(ctl->ring_empty[i]), 1);
   }
-  ptx::mbar_init(s.bar(ctl->mma_full), 1);
-  ptx::mbar_init(s.bar(ctl->ew_full), 4);
   ptx::mbar_init(s.bar(ctl->acc_full), 1);
   ptx::mbar_init(s.bar(ctl->s_full), 1);
   ptx::mbar_init(s.bar(ctl->dp_full), 1);
   ptx::mbar_init(s.bar(ctl->p_ready), 4);
   ptx::mbar_init(s.bar(ctl->ds_ready), 4);
-  ptx::mbar_init(s.bar(ctl->sb_full[0]), 1);
-  ptx::mbar_init(s.bar(ctl->sb_full[1]), 1);
   ptx::mbar_init(s.bar(ctl->vec_sync), 4);
   ptx::mbar_init(s.bar(ctl->epi_full), 4);
+  for (int t = 0; t < 2; ++t) {
+    ptx::mbar_init(s.bar(ctl->dq_s_full[t]), 1);
+    ptx::mbar_init(s.bar(ctl->dq_x_read[t]), 4);
+    ptx::mbar_init(s.bar(ctl->dq_dp_full[t]), 1);
+    ptx::mbar_init(s.bar(ctl->dq_ds_ready[t]), 4);
+  }
+  ptx::mbar_init(s.bar(ctl->dq_do_full), 1);
   ptx::mbar_init(s.bar(ctl->drain), 1);
   ctl->abort_flag = 0;
   ptx::fence_mbar_init();
@@ -290,36 +287,70 @@ __device__ __forceinline__ void stream_tiles(const Layout& L, const Sync& s, con
 }
 
 // ------------------------------------------------------------------ dQ kernel
-// TMEM: S double-buffered at [0,128) and [384,512) (KV tile j in buffer j&1, packed BF16 dS over
-// the upper 64 columns of its buffer), dP [128,256), dQ [256,384).
-constexpr uint32_t kColDP = 128, kColDQ = 256;
-__device__ __forceinline__ uint32_t col_sbuf(int j) { return (j & 1) ? 384u : 0u; }
+// One CTA per pair of 128-row Q tiles (a = 2p, b = 2p + 1) of one head.  Each streamed K/V tile
+// feeds six products (S, dP and dQ += dS K for both tiles) instead of three, which halves the
+// streamed bytes per product, and the tensor pipe runs one tile's products while the other
+// tile's elementwise warps work (the two-stage overlap of the forward kernel).
+// TMEM: X_a [0,128) and X_b [128,256) hold S, then dP over it once the elementwise warps have read
+// S, then packed BF16 dS over its lower 64 columns; dQ_a [256,384), dQ_b [384,512).
+// SMEM: Q_a, dO_a, Q_b, dO_b resident; a ring of two K tiles and one V tile.
+// Warps 0-3 elementwise for tile a, 4-7 for tile b, 8 TMA, 9 tcgen05.mma issue, 10-11 idle (the
+// register split below works on whole warpgroups).
+constexpr int kDqThreads = 384;
+constexpr int kDqLoadWarp = 8;
+constexpr int kDqMmaWarp = 9;
+// Register split (setmaxnreg): launched with 168 registers per thread (65536 / 384, rounded down
+// to the allocation unit; the host checks the compiled count), the two elementwise warpgroups
+// take 224 (a full 128-column row of P plus a 32-column chunk of dP), the third gives back to 56:
+// (2 * 224 + 56) * 128 == 168 * 384.
+constexpr uint32_t kDqRegLaunch = 168, kDqRegEw = 224, kDqRegMisc = 56;
+static_assert((2 * kDqRegEw + kDqRegMisc) * 128 == kDqRegLaunch * kDqThreads, "register split");
+constexpr int kDqKRing = 2;                        // ring slots 0..1: K tiles; slot 2: the V tile
+constexpr uint32_t kColDQ = 256;
+constexpr uint32_t kCtlOffsetDq = (4 + kDqKRing + 1) * kTileBytes;
+constexpr uint32_t kSmemBytesDq = kCtlOffsetDq + sizeof(SmemCtl);
+static_assert(kSmemBytesDq <= 227 * 1024, "dQ kernel shared memory exceeds a CTA's 227 KiB");
 
-__device__ __forceinline__ void dq_item(const Params& p, int& bh, int& qt, int& nkv) {
-  if (p.causal) {   // heaviest Q tiles first
-    qt = p.q_tiles - 1 - static_cast<int>(blockIdx.x) / p.bh;
+// Work of CTA blockIdx.x: head bh, first Q tile qa, K/V tiles n[t] each tile t of the pair sees
+// (0 for a tile past the end).  Causal: heaviest pairs first.
+__device__ __forceinline__ void dq_item(const Params& p, int& bh, int& qa, int (&n)[2]) {
+  const int pairs = (p.q_tiles + 1) >> 1;
+  int pr;
+  if (p.causal) {
+    pr = pairs - 1 - static_cast<int>(blockIdx.x) / p.bh;
     bh = static_cast<int>(blockIdx.x) % p.bh;
-    nkv = qt + 1 < p.kv_tiles ? qt + 1 : p.kv_tiles;
   } else {
-    bh = static_cast<int>(blockIdx.x) / p.q_tiles;
-    qt = static_cast<int>(blockIdx.x) % p.q_tiles;
-    nkv = p.kv_tiles;
+    bh = static_cast<int>(blockIdx.x) / pairs;
+    pr = static_cast<int>(blockIdx.x) % pairs;
+  }
+  qa = 2 * pr;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qt = qa + t;
+    n[t] = qt >= p.q_tiles ? 0 : (p.causal ? min(qt + 1, p.kv_tiles) : p.kv_tiles);
   }
 }
 
-// TMA warp of the dQ kernel: Q and dO resident, then K_j into the K ring and V_j into the V ring.
+// Ring slot r of the paired kernel (after the four resident tiles).
+__device__ __forceinline__ uint32_t dq_ring(const Layout& L, int r) { return L.ring(2 + r); }
+
+// TMA warp: Q_a, Q_b, K_0, dO_a, dO_b, V_0, then K_j, V_j for j = 1..nkv-1.
 __device__ __forceinline__ void dq_loads(const Layout& L, const Sync& s, const CUtensorMap* tm_q,
-                                         const CUtensorMap* tm_do, const CUtensorMap* tm_k,
-                                         const CUtensorMap* tm_v, int qrow, int nkv, int bh) {
+                                          const CUtensorMap* tm_do, const CUtensorMap* tm_k,
+                                          const CUtensorMap* tm_v, int qa, int ntiles, int nkv,
+                                          int bh) {
   SmemCtl* ctl = L.ctl;
-  if (s.lane == 0) {
-    const uint32_t fb = s.bar(ctl->fixed_full);
-    ptx::mbar_arrive_expect_tx(fb, 2 * kTileBytes);
-    load_tile(L.fixed(0), tm_q, fb, qrow, bh, L.heads4d);
-    load_tile(L.fixed(1), tm_do, fb, qrow, bh, L.heads4d);
-  }
-  __syncwarp();
-  int ks = 0, vs = 0;
+  auto fixed_pair = [&](const uint64_t& b, const CUtensorMap* tm, int first) {
+    if (s.lane == 0) {
+      const uint32_t fb = s.bar(b);
+      ptx::mbar_arrive_expect_tx(fb, ntiles * kTileBytes);
+      for (int t = 0; t < ntiles; ++t)
+        load_tile(L.fixed(2 * t + first), tm, fb, (qa + t) * kBlockM, bh, L.heads4d);
+    }
+    __syncwarp();
+  };
+  fixed_pair(ctl->fixed_full, tm_q, 0);
+  int ks = 0;
   uint32_t kph = 0, vph = 0, used = 0, last_par = 0;
   bool ok = true;
   auto load = [&](int slot, uint32_t ph, const CUtensorMap* tm, int row) -> bool {
@@ -327,7 +358,7 @@ __device__ __forceinline__ void dq_loads(const Layout& L, const Sync& s, const C
     if (s.lane == 0) {
       const uint32_t fb = s.bar(ctl->ring_full[slot]);
       ptx::mbar_arrive_expect_tx(fb, kTileBytes);
-      load_tile(L.ring(slot), tm, fb, row, bh, L.heads4d);
+      load_tile(dq_ring(L, slot), tm, fb, row, bh, L.heads4d);
     }
     __syncwarp();
     used |= 1u << slot;
@@ -337,20 +368,22 @@ __device__ __forceinline__ void dq_loads(const Layout& L, const Sync& s, const C
   for (int j = 0; ok && j < nkv; ++j) {
     if (!(ok = load(ks, kph, tm_k, j * kBlockN))) break;
     if (++ks == kDqKRing) { ks = 0; kph ^= 1u; }
-    if (!(ok = load(kDqKRing + vs, vph, tm_v, j * kBlockN))) break;
-    if (++vs == kDqVRing) { vs = 0; vph ^= 1u; }
+    if (j == 0) fixed_pair(ctl->dq_do_full, tm_do, 1);
+    if (!(ok = load(kDqKRing, vph, tm_v, j * kBlockN))) break;
+    vph ^= 1u;
   }
   if (!ok) {
-    for (int i = 0; i < kRing; ++i)
+    for (int i = 0; i <= kDqKRing; ++i)
       if ((used >> i) & 1u) s.drain_wait(ctl->ring_full[i], (last_par >> i) & 1u);
   }
   s.drain_wait(ctl->fixed_full, 0);
+  if (nkv > 0) s.drain_wait(ctl->dq_do_full, 0);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
 attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                   const Params p) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if ((ptx::smem_u32(smem_raw) & 1023u) != 0) {   // no room for realignment: skip the CTA
     if (threadIdx.x == 0) atomicOr(&g_attn_status, kStatusSmemAlign);
@@ -360,11 +393,12 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   SmemCtl* ctl = L.ctl;
   const uint32_t warp = threadIdx.x >> 5;
   Sync s{ctl, threadIdx.x & 31u};
-  int bh, qt, nkv;
-  dq_item(p, bh, qt, nkv);
+  int bh, qa, n[2];
+  dq_item(p, bh, qa, n);
+  const int nkv = n[0] > n[1] ? n[0] : n[1];
 
   if (threadIdx.x == 0) init_barriers(ctl, s);
-  if (warp == kMmaWarp) {
+  if (warp == kDqMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(&ctl->tmem_base), kTmemCols);
     ptx::tmem_relinquish();
   }
@@ -375,15 +409,16 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   const bool tmem_ok = tmem_alloc_base == kTmemBase;
   if (!tmem_ok && threadIdx.x == 0) atomicOr(&g_attn_status, kStatusTmemBase);
 
-  if (tmem_ok && warp == kLoadWarp) {
-    dq_loads(L, s, &tm_q, &tm_do, &tm_k, &tm_v, qt * kBlockM, nkv, bh);
-  } else if (tmem_ok && warp == kMmaWarp) {
-    // Per KV tile j the tensor pipe runs S(j+1) (into the other S buffer), dQ(j), dP(j+1): the
-    // elementwise work on tile j overlaps S(j+1), and dP(j+1) overwrites dP(j) only after the
-    // elementwise warps have read it (ds_ready).
+  if (tmem_ok && warp >= 8) ptx::setmaxnreg_dec<kDqRegMisc>();
+  if (tmem_ok && warp == kDqLoadWarp) {
+    dq_loads(L, s, &tm_q, &tm_do, &tm_k, &tm_v, qa, n[1] > 0 ? 2 : 1, nkv, bh);
+  } else if (tmem_ok && warp == kDqMmaWarp) {
+    // Per K/V tile j the tensor pipe runs dP_a(j), dP_b(j), dQ_a(j), S_a(j+1), dQ_b(j), S_b(j+1):
+    // S_t(j+1) reuses X_t once dQ_t(j) has read dS_t(j) (tcgen05.mma from one thread run in
+    // order), and a tile past its last K/V tile (causal) drops out.
     const bool leader = ptx::elect_one();
     bool ok = s.wait(ctl->fixed_full, 0, kStatusTimeoutMma);
-    int ks = 0, vs = 0;
+    int ks = 0;
     uint32_t kph = 0, vph = 0;
     auto next_k = [&](int& out) -> bool {
       out = ks;
@@ -391,114 +426,133 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       if (++ks == kDqKRing) { ks = 0; kph ^= 1u; }
       return r;
     };
-    auto next_v = [&](int& out) -> bool {
-      out = kDqKRing + vs;
-      const bool r = s.wait(ctl->ring_full[kDqKRing + vs], vph, kStatusTimeoutMma);
-      if (++vs == kDqVRing) { vs = 0; vph ^= 1u; }
-      return r;
-    };
-    auto issue_s = [&](int j, int kslot) {
+    auto issue_s = [&](int t, int kslot) {
       ptx::tc_fence_after();
       if (leader) {
-        mma_kmajor(kTmemBase + col_sbuf(j), L.fixed(0), L.ring(kslot));   // S = Q K^T
-        ptx::mma_commit(s.bar(ctl->sb_full[j & 1]));
+        mma_kmajor(kTmemBase + 128u * t, L.fixed(2 * t), dq_ring(L, kslot));   // S_t = Q_t K^T
+        ptx::mma_commit(s.bar(ctl->dq_s_full[t]));
       }
       __syncwarp();
     };
-    auto issue_dp = [&](int vslot) {
-      ptx::tc_fence_after();
-      if (leader) {
-        mma_kmajor(kTmemBase + kColDP, L.fixed(1), L.ring(vslot));   // dP = dO V^T
-        ptx::mma_commit(s.bar(ctl->dp_full));
-        ptx::mma_commit(s.bar(ctl->ring_empty[vslot]));
-      }
-      __syncwarp();
-    };
-    int kcur = 0, vslot = 0;
+    int kcur = 0;
     ok = ok && next_k(kcur);
-    if (ok) issue_s(0, kcur);
-    ok = ok && next_v(vslot);
-    if (ok) issue_dp(vslot);
+    if (ok) {
+      for (int t = 0; t < 2; ++t)
+        if (n[t] > 0) issue_s(t, kcur);
+    }
+    ok = ok && s.wait(ctl->dq_do_full, 0, kStatusTimeoutMma);
     for (int j = 0; ok && j < nkv; ++j) {
-      const bool more = j + 1 < nkv;
-      int knext = 0;
-      if (more) {
-        if (!(ok = next_k(knext))) break;
-        issue_s(j + 1, knext);
+      if (!(ok = s.wait(ctl->ring_full[kDqKRing], vph, kStatusTimeoutMma))) break;
+      vph ^= 1u;
+      for (int t = 0; ok && t < 2; ++t) {
+        if (j >= n[t]) continue;
+        if (!(ok = s.wait(ctl->dq_x_read[t], j & 1u, kStatusTimeoutMma))) break;
+        ptx::tc_fence_after();
+        if (leader) {
+          mma_kmajor(kTmemBase + 128u * t, L.fixed(2 * t + 1), dq_ring(L, kDqKRing));  // dP_t = dO_t V^T
+          ptx::mma_commit(s.bar(ctl->dq_dp_full[t]));
+        }
+        __syncwarp();
       }
-      if (!(ok = s.wait(ctl->ds_ready, j & 1u, kStatusTimeoutMma))) break;
-      ptx::tc_fence_after();
-      if (leader) {
-        mma_tmem_a(kTmemBase + kColDQ, kTmemBase + col_sbuf(j) + kColP, L.ring(kcur), j > 0);  // dQ += dS K
-        ptx::mma_commit(s.bar(ctl->ring_empty[kcur]));
-        if (!more) ptx::mma_commit(s.bar(ctl->acc_full));
-      }
+      if (!ok) break;
+      if (leader) ptx::mma_commit(s.bar(ctl->ring_empty[kDqKRing]));
       __syncwarp();
-      if (more) {
-        if (!(ok = next_v(vslot))) break;
-        issue_dp(vslot);
+      int knext = -1;
+      for (int t = 0; ok && t < 2; ++t) {
+        if (j >= n[t]) continue;
+        if (!(ok = s.wait(ctl->dq_ds_ready[t], j & 1u, kStatusTimeoutMma))) break;
+        ptx::tc_fence_after();
+        if (leader) {
+          mma_tmem_a(kTmemBase + kColDQ + 128u * t, kTmemBase + 128u * t, dq_ring(L, kcur), j > 0);  // dQ_t += dS_t K
+          if (t == 1 || j >= n[1]) ptx::mma_commit(s.bar(ctl->ring_empty[kcur]));
+        }
+        __syncwarp();
+        if (j + 1 < n[t]) {
+          if (knext < 0 && !(ok = next_k(knext))) break;
+          issue_s(t, knext);
+        }
       }
       kcur = knext;
     }
-    if (leader) ptx::mma_commit(s.bar(ctl->drain));
+    if (leader) {
+      if (ok) ptx::mma_commit(s.bar(ctl->acc_full));
+      ptx::mma_commit(s.bar(ctl->drain));
+    }
     __syncwarp();
     s.drain_wait(ctl->drain, 0);
-  } else if (tmem_ok && warp < 4) {
-    const uint32_t row_base = 32u * warp;
+  } else if (tmem_ok && warp < 8) {
+    ptx::setmaxnreg_inc<kDqRegEw>();
+    const int t = static_cast<int>(warp >> 2);
+    const uint32_t row_base = 32u * (warp & 3u);
     const int r = static_cast<int>(row_base + s.lane);
+    const int qt = qa + t;
     const int qrow = qt * kBlockM + r;
-    const bool row_ok = qrow < p.sq;
+    const bool row_ok = n[t] > 0 && qrow < p.sq;
     const size_t gi = static_cast<size_t>(bh) * p.sq + qrow;
     const float lse2 = row_ok ? static_cast<const float*>(p.lse)[gi] * 1.4426950408889634f : 0.f;
     const float dlt = row_ok ? p.delta[gi] : 0.f;
-    const uint32_t lane_off = row_base << 16;
+    const uint32_t x = kTmemBase + (row_base << 16) + 128u * t;
     bool ok = true;
-    for (int j = 0; ok && j < nkv; ++j) {
-      const uint32_t sb = kTmemBase + lane_off + col_sbuf(j);
-      if (!(ok = s.wait(ctl->sb_full[j & 1], (j >> 1) & 1u, kStatusTimeoutSoftmax))) break;
+    for (int j = 0; ok && j < n[t]; ++j) {
+      if (!(ok = s.wait(ctl->dq_s_full[t], j & 1u, kStatusTimeoutSoftmax))) break;
       ptx::tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ptx::tmem_ld_32x32b_x32(x + 32 * c, sr[c]);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      s.arrive(ctl->dq_x_read[t]);   // dP_t may now overwrite S_t
       int valid = kBlockN;
       if (j == p.kv_tiles - 1) valid = p.kv_valid_last;
       if (p.causal && j == qt) valid = min(valid, r + 1);
       // P = exp2(S * scale_log2 - LSE * log2 e), 0 past `valid`; kept in fp32 for dS.
-      float pf[4][32];
+      float2 pf[4][16];
+      const float2 sl2 = make_float2(p.scale_log2, p.scale_log2), nl = make_float2(-lse2, -lse2);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32];
-        ptx::tmem_ld_32x32b_x32(sb + 32 * c, sr);
-        ptx::tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float pv = ptx::ex2_ftz(fmaf(__uint_as_float(sr[i]), p.scale_log2, -lse2));
-          pf[c][i] = 32 * c + i < valid ? pv : 0.f;
+        for (int i = 0; i < 16; ++i) {
+          const float2 e = ptx::ffma2(
+              make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), sl2, nl);
+          pf[c][i].x = 32 * c + 2 * i < valid ? ptx::ex2_ftz(e.x) : 0.f;
+          pf[c][i].y = 32 * c + 2 * i + 1 < valid ? ptx::ex2_ftz(e.y) : 0.f;
         }
       }
-      // dS = P o (dP - delta), packed BF16 over the upper half of this S buffer (already read).
-      if (!(ok = s.wait(ctl->dp_full, j & 1u, kStatusTimeoutSoftmax))) break;
+      // dS = P o (dP - delta), packed BF16 into columns 16c..16c+15 once dP columns
+      // 32c..32c+31 are in registers: every column written has been read.  The load of the
+      // next 32 dP columns is in flight while a chunk is computed and stored.
+      if (!(ok = s.wait(ctl->dq_dp_full[t], j & 1u, kStatusTimeoutSoftmax))) break;
       ptx::tc_fence_after();
+      const float2 nd = make_float2(-dlt, -dlt);
+      uint32_t dr[2][32];
+      ptx::tmem_ld_32x32b_x32(x, dr[0]);
+      ptx::tmem_wait_ld_regs(dr[0]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t dr[32];
-        ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColDP + 32 * c, dr);
-        ptx::tmem_wait_ld();
+        if (c < 3) ptx::tmem_ld_32x32b_x32(x + 32 * (c + 1), dr[(c + 1) & 1]);
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = ptx::pack_bf16x2(pf[c][2 * i] * (__uint_as_float(dr[2 * i]) - dlt),
-                                   pf[c][2 * i + 1] * (__uint_as_float(dr[2 * i + 1]) - dlt));
-        ptx::tmem_st_32x32b_x16(sb + kColP + 16 * c, pk);
+        for (int i = 0; i < 16; ++i) {
+          const float2 d = ptx::fadd2(make_float2(__uint_as_float(dr[c & 1][2 * i]),
+                                                  __uint_as_float(dr[c & 1][2 * i + 1])), nd);
+          const float2 v = ptx::fmul2(pf[c][i], d);
+          pk[i] = ptx::pack_bf16x2(v.x, v.y);
+        }
+        ptx::tmem_st_32x32b_x16(x + 16 * c, pk);
+        if (c < 3) ptx::tmem_wait_ld_regs(dr[(c + 1) & 1]);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      s.arrive(ctl->ds_ready);
+      s.arrive(ctl->dq_ds_ready[t]);
     }
-    if (ok && s.wait(ctl->acc_full, 0, kStatusTimeoutSoftmax)) {
+    if (ok && n[t] > 0 && s.wait(ctl->acc_full, 0, kStatusTimeoutSoftmax)) {
       ptx::tc_fence_after();
       uint8_t* out = static_cast<uint8_t*>(p.out0) + row_offset(p, bh, qrow, p.sq);
+      const uint32_t acc_col = kTmemBase + (row_base << 16) + kColDQ + 128u * t;
 #pragma unroll 2
       for (int c = 0; c < 8; ++c) {
         uint32_t acc[16];
-        ptx::tmem_ld_32x32b_x16(kTmemBase + lane_off + kColDQ + 16 * c, acc);
+        ptx::tmem_ld_32x32b_x16(acc_col + 16 * c, acc);
         ptx::tmem_wait_ld();
         if (row_ok) store_cols16(out + 32 * c, acc, p.scale);
       }
@@ -507,7 +561,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kDqMmaWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_alloc_base, kTmemCols);
   }
@@ -635,11 +689,11 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const uint32_t lane_off = row_base << 16;
     const float* lse = static_cast<const float*>(p.lse) + static_cast<size_t>(bh) * p.sq;
     const float* dl = p.delta + static_cast<size_t>(bh) * p.sq;
-    // Column vectors (LSE*log2 e, delta) of Q tile i, staged by all 128 threads; masked query
-    // columns (past Sq) get LSE = +inf, so P = 0 there.
+    // Column vectors (-LSE*log2 e, delta) of Q tile i, staged by all 128 threads; masked query
+    // columns (past Sq) get -LSE = -inf, so P = 0 there.
     auto fetch = [&](int i, float& a, float& d) {
       const int qi = (q0 + i) * kBlockM + r;
-      a = qi < p.sq ? lse[qi] * 1.4426950408889634f : __int_as_float(0x7f800000);
+      a = qi < p.sq ? -(lse[qi] * 1.4426950408889634f) : __int_as_float(0xff800000);
       d = qi < p.sq ? dl[qi] : 0.f;
     };
     bool ok = true;
@@ -659,30 +713,35 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       const bool diag = p.causal && q0 + i == kt;   // query column c < key row r is masked
       const float* va = ctl->lse2[par];
       const float* vd = ctl->dlt[par];
-      // P^T = exp2(S^T * scale_log2 - LSE_col * log2 e), kept in fp32 for dS^T; high chunk
+      // P^T = exp2(S^T * scale_log2 + (-LSE_col * log2 e)), kept in fp32 for dS^T; high chunk
       // first, since the packed P^T of chunk c lands on S^T columns 64+16c.., already read.
-      float pf[4][32];
+      // The load of the next (lower) 32 columns is in flight while a chunk is computed.
+      const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+      float2 pf[4][16];
+      uint32_t xr[2][32];
+      ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColST + 96, xr[1]);
+      ptx::tmem_wait_ld_regs(xr[1]);
 #pragma unroll
       for (int c = 3; c >= 0; --c) {
-        uint32_t sr[32];
-        ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColST + 32 * c, sr);
-        ptx::tmem_wait_ld();
+        if (c > 0) ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColST + 32 * (c - 1), xr[(c - 1) & 1]);
         uint32_t pp[16];
 #pragma unroll
         for (int i2 = 0; i2 < 16; ++i2) {
           const int col = 32 * c + 2 * i2;
           const float2 a = *reinterpret_cast<const float2*>(va + col);
-          float p0 = ptx::ex2_ftz(fmaf(__uint_as_float(sr[2 * i2]), p.scale_log2, -a.x));
-          float p1 = ptx::ex2_ftz(fmaf(__uint_as_float(sr[2 * i2 + 1]), p.scale_log2, -a.y));
+          const float2 e = ptx::ffma2(make_float2(__uint_as_float(xr[c & 1][2 * i2]),
+                                                  __uint_as_float(xr[c & 1][2 * i2 + 1])), sl2, a);
+          float p0 = ptx::ex2_ftz(e.x);
+          float p1 = ptx::ex2_ftz(e.y);
           if (diag) {
             p0 = col < r ? 0.f : p0;
             p1 = col + 1 < r ? 0.f : p1;
           }
-          pf[c][2 * i2] = p0;
-          pf[c][2 * i2 + 1] = p1;
+          pf[c][i2] = make_float2(p0, p1);
           pp[i2] = ptx::pack_bf16x2(p0, p1);
         }
         ptx::tmem_st_32x32b_x16(kTmemBase + lane_off + kColST + kColP + 16 * c, pp);
+        if (c > 0) ptx::tmem_wait_ld_regs(xr[(c - 1) & 1]);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
@@ -690,19 +749,22 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       // dS^T = P^T o (dP^T - delta_col), packed over the upper half of dP^T the same way.
       if (!(ok = s.wait(ctl->dp_full, par, kStatusTimeoutSoftmax))) break;
       ptx::tc_fence_after();
+      ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColDPT + 96, xr[1]);
+      ptx::tmem_wait_ld_regs(xr[1]);
 #pragma unroll
       for (int c = 3; c >= 0; --c) {
-        uint32_t dr[32];
-        ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColDPT + 32 * c, dr);
-        ptx::tmem_wait_ld();
+        if (c > 0) ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColDPT + 32 * (c - 1), xr[(c - 1) & 1]);
         uint32_t pd[16];
 #pragma unroll
         for (int i2 = 0; i2 < 16; ++i2) {
           const float2 d = *reinterpret_cast<const float2*>(vd + 32 * c + 2 * i2);
-          pd[i2] = ptx::pack_bf16x2(pf[c][2 * i2] * (__uint_as_float(dr[2 * i2]) - d.x),
-                                    pf[c][2 * i2 + 1] * (__uint_as_float(dr[2 * i2 + 1]) - d.y));
+          const float2 v = ptx::fmul2(pf[c][i2],
+                                      ptx::fsub2(make_float2(__uint_as_float(xr[c & 1][2 * i2]),
+                                                             __uint_as_float(xr[c & 1][2 * i2 + 1])), d));
+          pd[i2] = ptx::pack_bf16x2(v.x, v.y);
         }
         ptx::tmem_st_32x32b_x16(kTmemBase + lane_off + kColDPT + kColP + 16 * c, pd);
+        if (c > 0) ptx::tmem_wait_ld_regs(xr[(c - 1) & 1]);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();

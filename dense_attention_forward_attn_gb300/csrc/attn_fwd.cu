@@ -47,11 +47,23 @@ int device_info(int dev, DeviceInfo* out) {
   }
   if (d.cc_major != 10 || d.cc_minor != 3) return ATTN_ERR_ARCH;
   if (d.smem_optin < static_cast<int>(attn::kSmemBytes)) return ATTN_ERR_ARCH;
+  // The kernels that split registers between warpgroups (setmaxnreg) need the block to be
+  // launched with exactly the per-thread count the split adds up to: with fewer, an increase
+  // could never be granted.  The compiled counts are checked once per device.
+  auto regs_are = [](const void* fn, int want) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return false;
+    return fa.numRegs == want;
+  };
   if (!d.attr_set) {
     if (cudaFuncSetAttribute(attn::attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(attn::kSmemBytes)) != cudaSuccess) {
       cudaGetLastError();
       return ATTN_ERR_CUDA;
+    }
+    if (!regs_are(reinterpret_cast<const void*>(attn::attn_fwd_kernel), 65536 / attn::kThreads)) {
+      cudaGetLastError();
+      return ATTN_ERR_UNSUPPORTED;
     }
     d.attr_set = true;
   }
@@ -63,6 +75,11 @@ int device_info(int dev, DeviceInfo* out) {
                              static_cast<int>(attn::bwd::kSmemBytesDkdv)) != cudaSuccess) {
       cudaGetLastError();
       return ATTN_ERR_CUDA;
+    }
+    if (!regs_are(reinterpret_cast<const void*>(attn::bwd::attn_bwd_dq_kernel),
+                  static_cast<int>(attn::bwd::kDqRegLaunch))) {
+      cudaGetLastError();
+      return ATTN_ERR_UNSUPPORTED;
     }
     d.bwd_attr_set = true;
   }
@@ -519,8 +536,9 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
                                                                       tm_dk, tm_dv, p);
   p.out0 = dq;
   p.out1 = nullptr;
-  attn::bwd::attn_bwd_dq_kernel<<<static_cast<unsigned>(bh * p.q_tiles), attn::bwd::kThreads,
-                                  attn::bwd::kSmemBytesDq, st>>>(tm_q, tm_k, tm_v, tm_do, p);
+  attn::bwd::attn_bwd_dq_kernel<<<static_cast<unsigned>(bh * ((p.q_tiles + 1) / 2)),
+                                  attn::bwd::kDqThreads, attn::bwd::kSmemBytesDq, st>>>(
+      tm_q, tm_k, tm_v, tm_do, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
