@@ -16,9 +16,10 @@
 // Every gradient is written by exactly one CTA (no atomics: deterministic).  dQ repeats the
 // S and dP products of dK/dV (7 tile products per tile pair instead of 5).
 //
-// Roles: dK/dV CTA (192 threads): warps 0-3 an elementwise warpgroup (one TMEM lane = one row
-// per thread), warp 4 TMA, warp 5 tcgen05.mma issue and TMEM allocation; dQ CTA (384 threads):
-// one elementwise warpgroup per Q tile, then a TMA and an MMA warp.  Tiles are staged by TMA
+// Roles: dK/dV CTA (320 threads): warps 0-7 two elementwise warpgroups (one TMEM lane = one key
+// row per thread, each warpgroup half of the query columns), warp 8 TMA, warp 9 tcgen05.mma
+// issue and TMEM allocation; dQ CTA (384 threads): one elementwise warpgroup per Q tile, then a
+// TMA and an MMA warp.  Tiles are staged by TMA
 // with 128-byte swizzle exactly as in the forward kernel; every mbarrier wait is bounded.
 #pragma once
 #include <cuda.h>
@@ -29,9 +30,9 @@
 namespace attn {
 namespace bwd {
 
-constexpr int kThreads = 192;
-constexpr int kLoadWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kThreads = 320;   // dK/dV kernel
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
 // Streamed tiles in flight.  dK/dV kernel: one ring of 4 slots (Q_i, dO_i alternate).  dQ kernel:
 // two K slots and one V slot (K_j lives from S_j to the last dQ += dS_j K_j, V_j only feeds the
 // dP_j products).
@@ -235,10 +236,10 @@ __device__ __forceinline__ void init_barriers(SmemCtl* ctl, const Sync& s) {
   ptx::mbar_init(s.bar(ctl->acc_full), 1);
   ptx::mbar_init(s.bar(ctl->s_full), 1);
   ptx::mbar_init(s.bar(ctl->dp_full), 1);
-  ptx::mbar_init(s.bar(ctl->p_ready), 4);
-  ptx::mbar_init(s.bar(ctl->ds_ready), 4);
-  ptx::mbar_init(s.bar(ctl->vec_sync), 4);
-  ptx::mbar_init(s.bar(ctl->epi_full), 4);
+  ptx::mbar_init(s.bar(ctl->p_ready), 8);
+  ptx::mbar_init(s.bar(ctl->ds_ready), 8);
+  ptx::mbar_init(s.bar(ctl->vec_sync), 8);
+  ptx::mbar_init(s.bar(ctl->epi_full), 8);
   for (int t = 0; t < 2; ++t) {
     ptx::mbar_init(s.bar(ctl->dq_s_full[t]), 1);
     ptx::mbar_init(s.bar(ctl->dq_x_read[t]), 4);
@@ -568,9 +569,11 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 }
 
 // ------------------------------------------------------------------ dK/dV kernel
-// TMEM: S^T [0,128) with packed BF16 P^T over 64..127, dP^T [128,256) with packed BF16 dS^T over
-// 192..255, dK [256,384), dV [384,512).
+// TMEM: S^T [0,128) with packed BF16 P^T over 32..95, dP^T [128,256) with packed BF16 dS^T over
+// 160..223, dK [256,384), dV [384,512).  The packed columns of query columns [64g, 64g+64) sit
+// inside S^T (dP^T) columns [64g, 64g+64), the ones elementwise warpgroup g reads.
 constexpr uint32_t kColST = 0, kColDPT = 128, kColDK = 256, kColDV = 384;
+constexpr uint32_t kColPT = 32;   // packed operand offset inside S^T and dP^T
 
 __device__ __forceinline__ void dkdv_item(const Params& p, int& bh, int& kt, int& q0, int& nq) {
   if (p.causal) {   // heaviest K/V tiles (earliest keys) first
@@ -645,7 +648,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       if (!(ok = s.wait(ctl->p_ready, i & 1u, kStatusTimeoutMma))) break;
       ptx::tc_fence_after();
       if (leader) {
-        mma_tmem_a(kTmemBase + kColDV, kTmemBase + kColST + kColP, L.ring(ds), i > 0);   // dV += P^T dO
+        mma_tmem_a(kTmemBase + kColDV, kTmemBase + kColST + kColPT, L.ring(ds), i > 0);   // dV += P^T dO
         ptx::mma_commit(s.bar(ctl->ring_empty[ds]));
       }
       __syncwarp();
@@ -662,7 +665,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       if (!(ok = s.wait(ctl->ds_ready, i & 1u, kStatusTimeoutMma))) break;
       ptx::tc_fence_after();
       if (leader) {
-        mma_tmem_a(kTmemBase + kColDK, kTmemBase + kColDPT + kColP, L.ring(qs), i > 0);  // dK += dS^T Q
+        mma_tmem_a(kTmemBase + kColDK, kTmemBase + kColDPT + kColPT, L.ring(qs), i > 0);  // dK += dS^T Q
         ptx::mma_commit(s.bar(ctl->ring_empty[qs]));
         if (!more) ptx::mma_commit(s.bar(ctl->acc_full));
       }
@@ -682,118 +685,128 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     if (leader) ptx::mma_commit(s.bar(ctl->drain));
     __syncwarp();
     s.drain_wait(ctl->drain, 0);
-  } else if (tmem_ok && warp < 4) {
-    const uint32_t row_base = 32u * warp;
+  } else if (tmem_ok && warp < 8) {
+    // Two elementwise warpgroups: warpgroup g works query columns [64g, 64g+64) of every key row
+    // (one TMEM lane per thread), so a pass is 64 columns per thread.
+    const int g = static_cast<int>(warp >> 2);
+    const uint32_t row_base = 32u * (warp & 3u);
     const int r = static_cast<int>(row_base + s.lane);   // key row within the tile
     const int krow = kt * kBlockN + r;
     const uint32_t lane_off = row_base << 16;
+    const int c0 = 64 * g;                               // this thread's first query column
     const float* lse = static_cast<const float*>(p.lse) + static_cast<size_t>(bh) * p.sq;
     const float* dl = p.delta + static_cast<size_t>(bh) * p.sq;
-    // Column vectors (-LSE*log2 e, delta) of Q tile i, staged by all 128 threads; masked query
-    // columns (past Sq) get -LSE = -inf, so P = 0 there.
-    auto fetch = [&](int i, float& a, float& d) {
+    // Column vectors of Q tile i, one value per thread: warpgroup 0 stages -LSE*log2 e of query
+    // column r, warpgroup 1 its delta; masked query columns (past Sq) get -LSE = -inf, so P = 0.
+    // The next tile's value is loaded a tile ahead from an in-range address and first used when
+    // it is staged, so the load's latency never stalls the warp.
+    const float* src = g == 0 ? lse : dl;
+    auto fetch = [&](int i) -> float {
       const int qi = (q0 + i) * kBlockM + r;
-      a = qi < p.sq ? -(lse[qi] * 1.4426950408889634f) : __int_as_float(0xff800000);
-      d = qi < p.sq ? dl[qi] : 0.f;
+      return src[qi < p.sq ? qi : p.sq - 1];
     };
+    auto stage = [&](int i, float raw) -> float {
+      const int qi = (q0 + i) * kBlockM + r;
+      if (g == 0) return qi < p.sq ? -(raw * 1.4426950408889634f) : __int_as_float(0xff800000);
+      return qi < p.sq ? raw : 0.f;
+    };
+    float* vec = g == 0 ? &ctl->lse2[0][0] : &ctl->dlt[0][0];
     bool ok = true;
-    float na = 0.f, nd = 0.f;
+    float nv = 0.f;
     if (nq > 0) {
-      fetch(0, na, nd);
-      ctl->lse2[0][r] = na;
-      ctl->dlt[0][r] = nd;
+      vec[r] = stage(0, fetch(0));
       s.arrive(ctl->vec_sync);
     }
+    const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+    const uint32_t st_cols = kTmemBase + lane_off + kColST, dpt_cols = kTmemBase + lane_off + kColDPT;
     for (int i = 0; ok && i < nq; ++i) {
       const int par = i & 1;
-      if (i + 1 < nq) fetch(i + 1, na, nd);   // next tile's vectors, in flight meanwhile
+      if (i + 1 < nq) nv = fetch(i + 1);   // next tile's vector, in flight meanwhile
       if (!(ok = s.wait(ctl->vec_sync, par, kStatusTimeoutSoftmax))) break;
       if (!(ok = s.wait(ctl->s_full, par, kStatusTimeoutSoftmax))) break;
       ptx::tc_fence_after();
       const bool diag = p.causal && q0 + i == kt;   // query column c < key row r is masked
-      const float* va = ctl->lse2[par];
-      const float* vd = ctl->dlt[par];
-      // P^T = exp2(S^T * scale_log2 + (-LSE_col * log2 e)), kept in fp32 for dS^T; high chunk
-      // first, since the packed P^T of chunk c lands on S^T columns 64+16c.., already read.
-      // The load of the next (lower) 32 columns is in flight while a chunk is computed.
-      const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
-      float2 pf[4][16];
+      const float* va = ctl->lse2[par] + c0;
+      const float* vd = ctl->dlt[par] + c0;
+      // P^T = exp2(S^T * scale_log2 + (-LSE_col * log2 e)), kept in fp32 for dS^T.  The packed
+      // BF16 P^T of columns c0.. lands on columns kColPT + c0/2.., inside this thread's own 64
+      // columns, written once all of them are in registers.
       uint32_t xr[2][32];
-      ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColST + 96, xr[1]);
+      ptx::tmem_ld_32x32b_x32(st_cols + c0, xr[0]);
+      ptx::tmem_ld_32x32b_x32(st_cols + c0 + 32, xr[1]);
+      ptx::tmem_wait_ld_regs(xr[0]);
       ptx::tmem_wait_ld_regs(xr[1]);
+      float2 pf[2][16];
 #pragma unroll
-      for (int c = 3; c >= 0; --c) {
-        if (c > 0) ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColST + 32 * (c - 1), xr[(c - 1) & 1]);
-        uint32_t pp[16];
+      for (int h = 0; h < 2; ++h) {
 #pragma unroll
         for (int i2 = 0; i2 < 16; ++i2) {
-          const int col = 32 * c + 2 * i2;
-          const float2 a = *reinterpret_cast<const float2*>(va + col);
-          const float2 e = ptx::ffma2(make_float2(__uint_as_float(xr[c & 1][2 * i2]),
-                                                  __uint_as_float(xr[c & 1][2 * i2 + 1])), sl2, a);
+          const int col = c0 + 32 * h + 2 * i2;
+          const float2 a = *reinterpret_cast<const float2*>(va + 32 * h + 2 * i2);
+          const float2 e = ptx::ffma2(make_float2(__uint_as_float(xr[h][2 * i2]),
+                                                  __uint_as_float(xr[h][2 * i2 + 1])), sl2, a);
           float p0 = ptx::ex2_ftz(e.x);
           float p1 = ptx::ex2_ftz(e.y);
           if (diag) {
             p0 = col < r ? 0.f : p0;
             p1 = col + 1 < r ? 0.f : p1;
           }
-          pf[c][i2] = make_float2(p0, p1);
-          pp[i2] = ptx::pack_bf16x2(p0, p1);
+          pf[h][i2] = make_float2(p0, p1);
         }
-        ptx::tmem_st_32x32b_x16(kTmemBase + lane_off + kColST + kColP + 16 * c, pp);
-        if (c > 0) ptx::tmem_wait_ld_regs(xr[(c - 1) & 1]);
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pp[16];
+#pragma unroll
+        for (int i2 = 0; i2 < 16; ++i2) pp[i2] = ptx::pack_bf16x2(pf[h][i2].x, pf[h][i2].y);
+        ptx::tmem_st_32x32b_x16(st_cols + kColPT + c0 / 2 + 16 * h, pp);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       s.arrive(ctl->p_ready);
-      // dS^T = P^T o (dP^T - delta_col), packed over the upper half of dP^T the same way.
+      // dS^T = P^T o (dP^T - delta_col), packed into the dP^T columns the same way.
       if (!(ok = s.wait(ctl->dp_full, par, kStatusTimeoutSoftmax))) break;
       ptx::tc_fence_after();
-      ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColDPT + 96, xr[1]);
+      ptx::tmem_ld_32x32b_x32(dpt_cols + c0, xr[0]);
+      ptx::tmem_ld_32x32b_x32(dpt_cols + c0 + 32, xr[1]);
+      ptx::tmem_wait_ld_regs(xr[0]);
       ptx::tmem_wait_ld_regs(xr[1]);
 #pragma unroll
-      for (int c = 3; c >= 0; --c) {
-        if (c > 0) ptx::tmem_ld_32x32b_x32(kTmemBase + lane_off + kColDPT + 32 * (c - 1), xr[(c - 1) & 1]);
+      for (int h = 0; h < 2; ++h) {
         uint32_t pd[16];
 #pragma unroll
         for (int i2 = 0; i2 < 16; ++i2) {
-          const float2 d = *reinterpret_cast<const float2*>(vd + 32 * c + 2 * i2);
-          const float2 v = ptx::fmul2(pf[c][i2],
-                                      ptx::fsub2(make_float2(__uint_as_float(xr[c & 1][2 * i2]),
-                                                             __uint_as_float(xr[c & 1][2 * i2 + 1])), d));
+          const float2 d = *reinterpret_cast<const float2*>(vd + 32 * h + 2 * i2);
+          const float2 v = ptx::fmul2(pf[h][i2],
+                                      ptx::fsub2(make_float2(__uint_as_float(xr[h][2 * i2]),
+                                                             __uint_as_float(xr[h][2 * i2 + 1])), d));
           pd[i2] = ptx::pack_bf16x2(v.x, v.y);
         }
-        ptx::tmem_st_32x32b_x16(kTmemBase + lane_off + kColDPT + kColP + 16 * c, pd);
-        if (c > 0) ptx::tmem_wait_ld_regs(xr[(c - 1) & 1]);
+        ptx::tmem_st_32x32b_x16(dpt_cols + kColPT + c0 / 2 + 16 * h, pd);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       s.arrive(ctl->ds_ready);
       if (i + 1 < nq) {
         // the other buffer was last read at tile i-1, whose dS^T the MMA warp has consumed
-        ctl->lse2[par ^ 1][r] = na;
-        ctl->dlt[par ^ 1][r] = nd;
+        vec[(par ^ 1) * kBlockM + r] = stage(i + 1, nv);
         s.arrive(ctl->vec_sync);
       }
     }
     const bool row_ok = krow < p.sk;
     const size_t gk = row_offset(p, bh, krow, p.sk);
-    uint8_t* dk = static_cast<uint8_t*>(p.out0) + gk;
-    uint8_t* dv = static_cast<uint8_t*>(p.out1) + gk;
     if (nq == 0) {
-      // keys no query attends (causal, Sk > Sq): zero gradients
-      if (row_ok) {
-        zero_row(dk);
-        zero_row(dv);
-      }
+      // keys no query attends (causal, Sk > Sq): zero gradients (dK by warpgroup 0, dV by 1)
+      if (row_ok) zero_row(static_cast<uint8_t*>(g == 0 ? p.out0 : p.out1) + gk);
     } else if (ok && s.wait(ctl->acc_full, 0, kStatusTimeoutSoftmax)) {
       // Every product is done, so the Q/dO ring is free: dK (ring slot 0) and dV (slot 1) are
-      // staged there as BF16 in the TMA layout (two 64-column slabs, 128-byte swizzle) and stored
-      // with four tensor copies (rows past Sk are clipped by the tensor maps).
+      // staged there as BF16 in the TMA layout (two 64-column slabs, 128-byte swizzle; warpgroup
+      // g fills slab g) and stored with four tensor copies (rows past Sk are clipped by the
+      // tensor maps).
       ptx::tc_fence_after();
       const uint32_t swz = static_cast<uint32_t>(r) & 7u;
 #pragma unroll 2
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 4 * g; c < 4 * g + 4; ++c) {
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           uint32_t acc[16];
@@ -836,7 +849,6 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       }
     }
   }
-
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
