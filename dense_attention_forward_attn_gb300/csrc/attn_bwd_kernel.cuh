@@ -186,6 +186,22 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* tm, u
   }
 }
 
+// Streamed Q/dO tiles of the dK/dV kernel are prefetched into L2 this many tiles ahead of their
+// loads (the K/V stream of the dQ kernel gains nothing from it).
+constexpr int kDkdvPrefetch = 2;
+
+// L2 prefetch of one 128-row tile (both 64-column boxes) of head bh.
+__device__ __forceinline__ void prefetch_tile(const CUtensorMap* tm, int row, int bh, int heads4d) {
+  if (heads4d) {
+    const int b = bh / heads4d, h = bh - b * heads4d;
+    ptx::tma_prefetch_4d(tm, 0, h, row, b);
+    ptx::tma_prefetch_4d(tm, 64, h, row, b);
+  } else {
+    ptx::tma_prefetch_3d(tm, 0, row, bh);
+    ptx::tma_prefetch_3d(tm, 64, row, bh);
+  }
+}
+
 // Byte offset of row `row` of head bh in a BF16 [B,H,S,128] or [B,S,H,128] tensor.
 __device__ __forceinline__ size_t row_offset(const Params& p, int bh, int row, int seq) {
   if (p.bshd) {
@@ -268,7 +284,16 @@ __device__ __forceinline__ void stream_tiles(const Layout& L, const Sync& s, con
   int slot = 0;
   uint32_t phase = 0, used = 0, last_par = 0;
   bool ok = true;
+  if (s.lane == 0)
+    for (int t = 1; t < kDkdvPrefetch && t < n; ++t) {
+      prefetch_tile(r0, (t0 + t) * kBlockM, bh, L.heads4d);
+      prefetch_tile(r1, (t0 + t) * kBlockM, bh, L.heads4d);
+    }
   for (int t = 0; ok && t < 2 * n; ++t) {
+    if ((t & 1) && s.lane == 0 && (t >> 1) + kDkdvPrefetch < n) {
+      prefetch_tile(r0, (t0 + (t >> 1) + kDkdvPrefetch) * kBlockM, bh, L.heads4d);
+      prefetch_tile(r1, (t0 + (t >> 1) + kDkdvPrefetch) * kBlockM, bh, L.heads4d);
+    }
     if (!(ok = s.wait(ctl->ring_empty[slot], phase ^ 1u, kStatusTimeoutLoad))) break;
     if (s.lane == 0) {
       const uint32_t fb = s.bar(ctl->ring_full[slot]);
