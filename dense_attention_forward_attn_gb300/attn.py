@@ -226,24 +226,49 @@ def fwd(q, k, v, scale: float | None = None, return_lse: bool = True, causal: bo
 _side_streams = {}
 
 
-def fwd_host_batch(problems):
+def _flop_per_byte(pb):
+    """Tensor-core work per byte copied for one host-buffer problem: 4*Sq*Sk*D FLOP (half with
+    the causal mask) over the BF16 Q, K, V in and O out."""
+    try:
+        B, H, Sq, Sk, D = _dims(pb["q"], pb["k"], pb.get("layout", "bhsd"))
+    except (ValueError, TypeError, AttributeError, KeyError):
+        return 0.0   # malformed; the enqueue reports it
+    flop = 4.0 * Sq * Sk * D * (0.5 if pb.get("causal", False) else 1.0)
+    return flop / max(1, 2 * D * (2 * Sq + 2 * Sk))
+
+
+def batch_order(problems):
+    """The order fwd_host_batch enqueues problems in by default: most tensor work per copied byte
+    first (stable for ties)."""
+    return sorted(range(len(problems)), key=lambda i: -_flop_per_byte(problems[i]))
+
+
+def fwd_host_batch(problems, order=None):
     """Several host-buffer forwards at once: each problem is a dict with q, k, v (CPU BF16) and
     optional scale, causal, layout, return_lse.  Each goes through attn_fwd_host on its own side
-    stream (after the work already on the current stream), so one problem's copies overlap the
-    others' kernels; returns [(o, lse)] (pinned CPU tensors) once all are complete."""
+    stream (after the work already on the current stream); the library's copies run in the
+    order the problems are enqueued, so by default the problems with the most tensor work per
+    copied byte go first: their kernels then run while the copies of the others stream in,
+    instead of after the last copy.  `order` (a permutation of range(len(problems))) overrides
+    that.  Returns [(o, lse)] (pinned CPU tensors) in the problems' order, once all are
+    complete."""
     import torch
+    order = batch_order(problems) if order is None else list(order)
+    if sorted(order) != list(range(len(problems))):
+        raise ValueError("order must be a permutation of the problem indices")
     dev = torch.device("cuda", torch.cuda.current_device())
     cur = torch.cuda.current_stream(dev)
     streams = _side_streams.setdefault(dev.index, [])
     while len(streams) < len(problems):
         streams.append(torch.cuda.Stream(dev))
-    pending = []
-    for pb, st in zip(problems, streams):
+    pending = [None] * len(problems)
+    for i, st in zip(order, streams):
+        pb = problems[i]
         st.wait_stream(cur)
         with torch.cuda.stream(st):
-            pending.append(_fwd_host_enqueue(pb["q"], pb["k"], pb["v"], pb.get("scale"),
-                                             pb.get("return_lse", True), pb.get("causal", False),
-                                             pb.get("layout", "bhsd")))
+            pending[i] = _fwd_host_enqueue(pb["q"], pb["k"], pb["v"], pb.get("scale"),
+                                           pb.get("return_lse", True), pb.get("causal", False),
+                                           pb.get("layout", "bhsd"))
     for st in streams[:len(problems)]:
         cur.wait_stream(st)
     cur.synchronize()

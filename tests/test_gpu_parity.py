@@ -386,8 +386,9 @@ def test_host_buffer_batch_matches_single_calls():
         problems.append(dict(q=tens[0], k=tens[1], v=tens[2], scale=0.09, causal=causal, layout=layout))
         o_d, lse_d = attn.fwd(*(t.cuda() for t in tens), scale=0.09, causal=causal, layout=layout)
         expect.append((o_d.cpu(), lse_d.cpu()))
-    for rep in range(2):
-        got = attn.fwd_host_batch(problems)
+    # the default order (most work per copied byte first) and two explicit ones
+    for order in (None, [0, 1, 2], [2, 0, 1]):
+        got = attn.fwd_host_batch(problems, order=order)
         for (o, lse), (o_e, lse_e) in zip(got, expect):
             assert torch.equal(o, o_e) and torch.equal(lse, lse_e)
     assert attn.device_status() == 0

@@ -236,3 +236,22 @@ def test_host_workspace_bytes(lib):
     assert ws.value == al(q) + 2 * al(kv) + al(q) + al(l)
     assert lib.attn_fwd_host_workspace(2, 3, 300, 500, 64, 0, ctypes.byref(ws)) == attn.ATTN_ERR_UNSUPPORTED
     assert lib.attn_fwd_host_workspace(2, 3, 300, 500, 128, 8, ctypes.byref(ws)) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_host_batch_order_puts_most_work_per_byte_first():
+    """fwd_host_batch's default enqueue order: problems with more tensor work per copied byte
+    first, so their kernels run while the other problems' copies stream in; a bad explicit
+    order is rejected before any CUDA call."""
+    import torch
+    def pb(B, H, Sq, Sk, causal=False, layout="bhsd"):
+        qs = (B, Sq, H, 128) if layout == "bshd" else (B, H, Sq, 128)
+        ks = (B, Sk, H, 128) if layout == "bshd" else (B, H, Sk, 128)
+        z = lambda sh: torch.empty(sh, dtype=torch.bfloat16)
+        return dict(q=z(qs), k=z(ks), v=z(ks), causal=causal, layout=layout)
+    probs = [pb(4, 16, 64, 64), pb(1, 16, 256, 256), pb(2, 16, 128, 128)]
+    assert attn.batch_order(probs) == [1, 2, 0]
+    # the causal mask halves the work: S=256 causal ranks with S=128 dense (stable order)
+    probs = [pb(1, 2, 128, 128), pb(1, 2, 256, 256, causal=True), pb(1, 2, 64, 64, layout="bshd")]
+    assert attn.batch_order(probs) == [0, 1, 2]
+    with pytest.raises(ValueError):
+        attn.fwd_host_batch(probs, order=[0, 0, 1])
