@@ -10,7 +10,7 @@ BF16 peak.  Every input set (Q+K+V = 192 MiB per shape) is larger than the
 129 MB L2, so no explicit flush is needed between timed iterations.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--row dense|causal|bshd|backward|backward-causal]
+                  [--row dense|causal|bshd|soft-exp2|backward|backward-causal]
 
 --row (default dense, the headline above) times the same sweep on one of the
 other built rows instead: the causal forward (half of 4*B*H*S^2*D counted),
@@ -54,6 +54,9 @@ ROWS = {
                "S=4K/8K/16K sweep (B=4/2/1, H=16, D=128, BF16, causal top-left)", 0.5),
     "bshd": ("attention fwd TFLOPS (4·B·H·S²·D), [B,S,H,D] tensors, at S=4K/8K/16K",
              "S=4K/8K/16K sweep (B=4/2/1, H=16, D=128, BF16, non-causal, BSHD layout)", 1.0),
+    "soft-exp2": ("attention fwd TFLOPS (4·B·H·S²·D), 4/16 of P by software exp2, at S=4K/8K/16K",
+                  "S=4K/8K/16K sweep (B=4/2/1, H=16, D=128, BF16, non-causal, ATTN_FLAG_SOFT_EXP2)",
+                  1.0),
     "backward": ("attention bwd TFLOPS (2.5 × 4·B·H·S²·D) at S=4K/8K/16K",
                  "S=4K/8K/16K sweep (B=4/2/1, H=16, D=128, BF16, non-causal), dQ/dK/dV", 2.5),
     "backward-causal": ("attention bwd TFLOPS, causal (1.25 × 4·B·H·S²·D) at S=4K/8K/16K",
@@ -250,6 +253,7 @@ def run_ours(args):
     metric, workload, flop_factor = ROWS[row]
     causal = row in ("causal", "backward-causal")
     layout = "bshd" if row == "bshd" else "bhsd"
+    soft = row == "soft-exp2"
     backward = row.startswith("backward")
     shapes = []
     for w in wl.HEADLINE:
@@ -278,7 +282,8 @@ def run_ours(args):
 
     def one(w, d, o, lse, extra):
         if not backward:
-            attn.fwd_into(d[0], d[1], d[2], o, lse, w.scale, causal=causal, layout=layout)
+            attn.fwd_into(d[0], d[1], d[2], o, lse, w.scale, causal=causal, layout=layout,
+                          soft_exp2=soft)
             return
         dout, dq, dk, dv, delta = extra
         rc = lib.attn_bwd(d[0].data_ptr(), d[1].data_ptr(), d[2].data_ptr(), o.data_ptr(),
@@ -347,7 +352,8 @@ def run_ours(args):
         h2d = sum(sum(t.numel() * t.element_size() for t in host) for _, _, host, *_ in shapes)
         d2h = sum(o.numel() * o.element_size() + lse.numel() * 4 for *_, o, lse, _x in shapes)
         e2e_steps = max(2, min(args.steps, 10))
-        problems = [dict(q=host[0], k=host[1], v=host[2], scale=w.scale, causal=causal, layout=layout)
+        problems = [dict(q=host[0], k=host[1], v=host[2], scale=w.scale, causal=causal, layout=layout,
+                         soft_exp2=soft)
                     for w, _, host, *_ in shapes]
         for _ in range(max(3, args.warmup)):   # warm-up: pinned output buffers, side streams
             results = attn.fwd_host_batch(problems)

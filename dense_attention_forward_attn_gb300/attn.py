@@ -25,6 +25,7 @@ ATTN_ERR_CUDA = -4
 ATTN_ERR_TOO_LARGE = -5
 ATTN_FLAG_CAUSAL = 1
 ATTN_FLAG_BSHD = 2
+ATTN_FLAG_SOFT_EXP2 = 4           # forward: 4 of 16 P columns by polynomial exp2 (Chapter 9)
 ATTN_FLAG_TEST_WITHHOLD = 0x100   # test hook: see include/attn_fwd.h
 
 
@@ -103,10 +104,11 @@ def status_string(status: int) -> str:
     return library().attn_status_string(int(status)).decode()
 
 
-def _flags(causal: bool, layout: str = "bhsd") -> int:
+def _flags(causal: bool, layout: str = "bhsd", soft_exp2: bool = False) -> int:
     if layout not in ("bhsd", "bshd"):
         raise ValueError("layout must be 'bhsd' ([B,H,S,D]) or 'bshd' ([B,S,H,D])")
-    return (ATTN_FLAG_CAUSAL if causal else 0) | (ATTN_FLAG_BSHD if layout == "bshd" else 0)
+    return ((ATTN_FLAG_CAUSAL if causal else 0) | (ATTN_FLAG_BSHD if layout == "bshd" else 0)
+            | (ATTN_FLAG_SOFT_EXP2 if soft_exp2 else 0))
 
 
 def plan(B: int, H: int, Sq: int, Sk: int, D: int = 128, num_sms: int = 0,
@@ -172,14 +174,14 @@ def _dims(q, k, layout):
 
 
 def fwd_into(q, k, v, o, lse=None, scale: float | None = None, stream=None,
-             causal: bool = False, layout: str = "bhsd") -> None:
+             causal: bool = False, layout: str = "bhsd", soft_exp2: bool = False) -> None:
     """Device tensors only: write softmax(scale q k^T) v into `o` (and LSE into `lse`).
 
     layout "bhsd": q/o [B,H,Sq,D], k/v [B,H,Sk,D]; "bshd": q/o [B,Sq,H,D], k/v [B,Sk,H,D].
-    lse is [B,H,Sq] either way.
+    lse is [B,H,Sq] either way.  soft_exp2: ATTN_FLAG_SOFT_EXP2 (off by default).
     """
     import torch
-    flags = _flags(causal, layout)
+    flags = _flags(causal, layout, soft_exp2)
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
         _check(t, n)
     B, H, Sq, Sk, D = _dims(q, k, layout)
@@ -201,7 +203,7 @@ def fwd_into(q, k, v, o, lse=None, scale: float | None = None, stream=None,
 
 
 def fwd(q, k, v, scale: float | None = None, return_lse: bool = True, causal: bool = False,
-        layout: str = "bhsd"):
+        layout: str = "bhsd", soft_exp2: bool = False):
     """Attention forward.  q [B,H,Sq,D], k/v [B,H,Sk,D] (or [B,S,H,D] with layout="bshd"),
     BF16 contiguous.  Returns (o in q's layout, lse [B,H,Sq] or None).
 
@@ -216,10 +218,10 @@ def fwd(q, k, v, scale: float | None = None, return_lse: bool = True, causal: bo
         _check(t, n)
     B, H, Sq, Sk, D = _dims(q, k, layout)
     if not q.is_cuda:
-        return _fwd_host(q, k, v, B, H, Sq, Sk, D, scale, return_lse, causal, layout)
+        return _fwd_host(q, k, v, B, H, Sq, Sk, D, scale, return_lse, causal, layout, soft_exp2)
     o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device) if return_lse else None
-    fwd_into(q, k, v, o, lse, scale, causal=causal, layout=layout)
+    fwd_into(q, k, v, o, lse, scale, causal=causal, layout=layout, soft_exp2=soft_exp2)
     return o, lse
 
 
@@ -245,8 +247,8 @@ def batch_order(problems):
 
 def fwd_host_batch(problems, order=None):
     """Several host-buffer forwards at once: each problem is a dict with q, k, v (CPU BF16) and
-    optional scale, causal, layout, return_lse.  Each goes through attn_fwd_host on its own side
-    stream (after the work already on the current stream); the library's copies run in the
+    optional scale, causal, layout, soft_exp2, return_lse.  Each goes through attn_fwd_host on its
+    own side stream (after the work already on the current stream); the library's copies run in the
     order the problems are enqueued, so by default the problems with the most tensor work per
     copied byte go first: their kernels then run while the copies of the others stream in,
     instead of after the last copy.  `order` (a permutation of range(len(problems))) overrides
@@ -268,22 +270,22 @@ def fwd_host_batch(problems, order=None):
         with torch.cuda.stream(st):
             pending[i] = _fwd_host_enqueue(pb["q"], pb["k"], pb["v"], pb.get("scale"),
                                            pb.get("return_lse", True), pb.get("causal", False),
-                                           pb.get("layout", "bhsd"))
+                                           pb.get("layout", "bhsd"), pb.get("soft_exp2", False))
     for st in streams[:len(problems)]:
         cur.wait_stream(st)
     cur.synchronize()
     return [(o, lse) for o, lse, _keep in pending]
 
 
-def _fwd_host(q, k, v, B, H, Sq, Sk, D, scale, return_lse, causal, layout):
+def _fwd_host(q, k, v, B, H, Sq, Sk, D, scale, return_lse, causal, layout, soft_exp2=False):
     import torch
-    o, lse, keep = _fwd_host_enqueue(q, k, v, scale, return_lse, causal, layout)
+    o, lse, keep = _fwd_host_enqueue(q, k, v, scale, return_lse, causal, layout, soft_exp2)
     torch.cuda.current_stream().synchronize()
     del keep
     return o, lse
 
 
-def _fwd_host_enqueue(q, k, v, scale, return_lse, causal, layout):
+def _fwd_host_enqueue(q, k, v, scale, return_lse, causal, layout, soft_exp2=False):
     """Enqueue attn_fwd_host on the current stream; returns (o, lse, keep) -- keep (the device
     workspace and the pinned inputs) must stay referenced until the stream has finished the
     call, since the library's copies are not tracked by PyTorch's allocators."""
@@ -296,7 +298,7 @@ def _fwd_host_enqueue(q, k, v, scale, return_lse, causal, layout):
     kv_shape = (B, Sk, H, D) if layout == "bshd" else (B, H, Sk, D)
     if tuple(k.shape) != kv_shape or tuple(v.shape) != kv_shape:
         raise ValueError("shape mismatch between q, k, v")
-    flags = _flags(causal, layout)
+    flags = _flags(causal, layout, soft_exp2)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     q, k, v = (t if t.is_pinned() else t.pin_memory() for t in (q, k, v))

@@ -56,12 +56,15 @@ int device_info(int dev, DeviceInfo* out) {
     return fa.numRegs == want;
   };
   if (!d.attr_set) {
-    if (cudaFuncSetAttribute(attn::attn_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn::attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(attn::kSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(attn::attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(attn::kSmemBytes)) != cudaSuccess) {
       cudaGetLastError();
       return ATTN_ERR_CUDA;
     }
-    if (!regs_are(reinterpret_cast<const void*>(attn::attn_fwd_kernel), 65536 / attn::kThreads)) {
+    if (!regs_are(reinterpret_cast<const void*>(attn::attn_fwd_kernel<false>), 65536 / attn::kThreads) ||
+        !regs_are(reinterpret_cast<const void*>(attn::attn_fwd_kernel<true>), 65536 / attn::kThreads)) {
       cudaGetLastError();
       return ATTN_ERR_UNSUPPORTED;
     }
@@ -277,8 +280,12 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
   p.test_withhold = (flags & ATTN_FLAG_TEST_WITHHOLD) ? 1 : 0;
   const int grid = p.num_items < info.num_sms ? p.num_items : info.num_sms;
 
-  attn::attn_fwd_kernel<<<grid, attn::kThreads, attn::kSmemBytes,
-                          static_cast<cudaStream_t>(stream)>>>(tm_q, tm_k, tm_v, p);
+  if (flags & ATTN_FLAG_SOFT_EXP2)
+    attn::attn_fwd_kernel<true><<<grid, attn::kThreads, attn::kSmemBytes,
+                                  static_cast<cudaStream_t>(stream)>>>(tm_q, tm_k, tm_v, p);
+  else
+    attn::attn_fwd_kernel<false><<<grid, attn::kThreads, attn::kSmemBytes,
+                                   static_cast<cudaStream_t>(stream)>>>(tm_q, tm_k, tm_v, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
@@ -449,7 +456,7 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
                         const void* dout, const float* lse, void* dq, void* dk, void* dv,
                         float* delta, int B, int H, int Sq, int Sk, int D, float scale, int flags,
                         void* stream) {
-  if (flags & ~ATTN_FLAGS_ALL) return ATTN_ERR_INVALID_ARG;
+  if (flags & ~(ATTN_FLAG_CAUSAL | ATTN_FLAG_BSHD)) return ATTN_ERR_INVALID_ARG;
   int rc = check_shape(B, H, Sq, Sk, D);
   if (rc != ATTN_OK) return rc;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;

@@ -24,6 +24,10 @@
 //     is issued as soon as its Q tile and first K tile are resident.
 //   * Chapter 8: base-2 exponentials with the scale folded into log2(e), the row
 //     max taken on raw scores, ex2.approx.ftz.
+//   * Chapter 9 (optional, ATTN_FLAG_SOFT_EXP2; a second instantiation of the
+//     kernel): 4 of every 16 P columns take a polynomial exp2 on the FMA and
+//     integer pipes instead of MUFU.  On GB300 the default all-MUFU path is
+//     faster (MUFU does 32 exp2 per cycle per SM), so it is off by default.
 //   * Chapter 11: the kept row max is replaced only when a tile's max exceeds it
 //     by at least 8 (base-2 units); otherwise P is taken against the stale max.
 //   * Chapter 13 splits P*V to start it before all of P is written; here P*V is
@@ -560,6 +564,29 @@ __device__ __forceinline__ void mask_scores(uint32_t (&sr)[4][32], int valid, ui
 // TMEM over the upper half of this stage's S columns, published once all 128 are written
 // (p_full).  Masked columns arrive as -inf and come out as 0.  Returns the row sum of the tile's
 // fp32 P.
+// 2^x for two values on the FMA and integer pipes, no MUFU ("B200 Attention Kernel from Scratch to
+// Near-SOTA in 60 Diagrams", Chapter 9 and its appendix on the approximation): x = n + f with
+// n = floor(x), f in [0, 1); 2^f by the cubic minimax fit of 2^f on [0, 1] with p(0) = 1 (relative
+// error 8.6e-5; coefficients from soft_exp2_fit.py); n is added to the exponent field.  x is
+// clamped at -127, where the result is below the normal range (the hardware path flushes it).
+constexpr float kExp2C1 = 0.69511676f, kExp2C2 = 0.227645f, kExp2C3 = 0.07706704f;
+__device__ __forceinline__ float2 soft_exp2x2(float2 x) {
+  constexpr float kRound = 12582912.0f;   // 1.5 * 2^23: x + kRound, rounded down, is kRound + n
+  x.x = fmaxf(x.x, -127.0f);
+  x.y = fmaxf(x.y, -127.0f);
+  const float2 rr = make_float2(kRound, kRound);
+  const float2 t = ptx::fadd2_rm(x, rr);
+  const float2 f = ptx::fsub2(x, ptx::fsub2(t, rr));
+  float2 y = ptx::ffma2(make_float2(kExp2C3, kExp2C3), f, make_float2(kExp2C2, kExp2C2));
+  y = ptx::ffma2(y, f, make_float2(kExp2C1, kExp2C1));
+  y = ptx::ffma2(y, f, make_float2(1.0f, 1.0f));
+  const int bias = __float_as_int(kRound);
+  y.x = __int_as_float(__float_as_int(y.x) + ((__float_as_int(t.x) - bias) << 23));
+  y.y = __int_as_float(__float_as_int(y.y) + ((__float_as_int(t.y) - bias) << 23));
+  return y;
+}
+
+template <bool kSoftExp2>
 __device__ __forceinline__ float produce_p(const Ctx& c, int q, const uint32_t (&sr)[4][32],
                                            float scale_log2, float m_kept, uint32_t taddr_s) {
   SmemCtl* ctl = c.ctl;
@@ -574,8 +601,12 @@ __device__ __forceinline__ float produce_p(const Ctx& c, int q, const uint32_t (
     for (int i = 0; i < 16; ++i) {
       float2 x = ptx::ffma2(make_float2(__uint_as_float(sr[cc][2 * i]), __uint_as_float(sr[cc][2 * i + 1])),
                             c2, nm2);
-      x.x = ptx::ex2_ftz(x.x);
-      x.y = ptx::ex2_ftz(x.y);
+      if (kSoftExp2 && (i & 7) >= 6) {   // columns 12..15 of every 16 (Chapter 9's split)
+        x = soft_exp2x2(x);
+      } else {
+        x.x = ptx::ex2_ftz(x.x);
+        x.y = ptx::ex2_ftz(x.y);
+      }
       if (i & 1) acc1 = ptx::fadd2(acc1, x); else acc0 = ptx::fadd2(acc0, x);
       pk[i] = ptx::pack_bf16x2(x.x, x.y);
     }
@@ -645,6 +676,7 @@ __device__ __forceinline__ void epilogue_store(const Params& p, int q, const Wor
     p.lse[static_cast<size_t>(w.bh) * p.sq + grow] = (m + log2f(l)) * 0.69314718055994530942f;
 }
 
+template <bool kSoftExp2>
 __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int q) {
   SmemCtl* ctl = c.ctl;
   const uint32_t row_base = 32u * (c.warp & 3u);
@@ -709,7 +741,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
       ctl->alpha[q][tphase][row] = alpha;
       c.arrive(ctl->stats_full[q]);
 
-      l += produce_p(c, q, sr, scale_log2, m_kept, taddr_s);
+      l += produce_p<kSoftExp2>(c, q, sr, scale_log2, m_kept, taddr_s);
       tphase ^= 1u;
     }
     have_prev = true;
@@ -769,6 +801,7 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
 }
 
 // ------------------------------------------------------------------ kernel
+template <bool kSoftExp2>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -817,7 +850,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (threadIdx.x == 0) atomicOr(&g_attn_status, kStatusTmemBase);
   } else if (c.warp < kCorrWarp0) {
     ptx::setmaxnreg_inc<kRegSoftmax>();
-    softmax_role(c, p, static_cast<int>(c.warp >> 2));
+    softmax_role<kSoftExp2>(c, p, static_cast<int>(c.warp >> 2));
   } else if (c.warp < kLoadWarp) {
     ptx::setmaxnreg_dec<kRegCorr>();
     correction_role(c, p);

@@ -82,7 +82,12 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  * attn_device_status) and exits, leaving its outputs unspecified.  For testing the failure path;
  * other CTAs and later calls are unaffected. */
 #define ATTN_FLAG_TEST_WITHHOLD 0x100
-#define ATTN_FLAGS_ALL (ATTN_FLAG_CAUSAL | ATTN_FLAG_BSHD | ATTN_FLAG_TEST_WITHHOLD)
+/* Forward only: 4 of every 16 P columns use a polynomial exp2 on the FMA and integer pipes
+ * instead of the MUFU unit ("B200 Attention Kernel from Scratch to Near-SOTA in 60 Diagrams",
+ * Chapter 9; relative error of that exp2 <= 1e-4).  Off by default: slower on GB300. */
+#define ATTN_FLAG_SOFT_EXP2 4
+#define ATTN_FLAGS_ALL \
+  (ATTN_FLAG_CAUSAL | ATTN_FLAG_BSHD | ATTN_FLAG_SOFT_EXP2 | ATTN_FLAG_TEST_WITHHOLD)
 
 /*
  * attn_fwd_ex -- attn_fwd with options.  Arguments, ownership, errors and
@@ -167,7 +172,8 @@ int attn_fwd_host_chunking(int B, int H, int Sq, int Sk, int flags, int num_sms,
  *   lse              device, fp32, [B, H, Sq], read (attn_fwd's lse), either layout
  *   delta            device, fp32, [B, H, Sq]: scratch owned by the caller, written
  *                    with delta_i and read back by the same call
- *   flags            ATTN_FLAG_CAUSAL (must match the forward) and/or ATTN_FLAG_BSHD
+ *   flags            ATTN_FLAG_CAUSAL (must match the forward) and/or ATTN_FLAG_BSHD;
+ *                    any other bit gives ATTN_ERR_INVALID_ARG
  *
  * Sizes, scale, alignment (16 bytes for BF16 tensors, 4 for lse and delta),
  * ownership and error rules as attn_fwd; no output may overlap any input or

@@ -141,11 +141,12 @@ def test_flags_are_checked(lib):
     big = 1 << 40
     vp = ctypes.c_void_p
     rc = lib.attn_fwd_ex(vp(big), vp(2 * big), vp(3 * big), vp(4 * big), None, 1, 1, 128, 128,
-                         128, 0.1, 4, None)
+                         128, 0.1, 8, None)   # bit 3 is not a flag
     assert rc == attn.ATTN_ERR_INVALID_ARG
     with pytest.raises(ValueError):
         attn._flags(False, "sbhd")
     assert attn._flags(True, "bshd") == attn.ATTN_FLAG_CAUSAL | attn.ATTN_FLAG_BSHD
+    assert attn._flags(False, "bhsd", soft_exp2=True) == attn.ATTN_FLAG_SOFT_EXP2
 
 
 def test_empty_problems_are_ok_without_launch(lib):
