@@ -567,12 +567,13 @@ __device__ __forceinline__ void mask_scores(uint32_t (&sr)[4][32], int valid, ui
 // 2^x for two values on the FMA and integer pipes, no MUFU ("B200 Attention Kernel from Scratch to
 // Near-SOTA in 60 Diagrams", Chapter 9 and its appendix on the approximation): x = n + f with
 // n = floor(x), f in [0, 1); 2^f by the cubic minimax fit of 2^f on [0, 1] with p(0) = 1 (relative
-// error 8.6e-5; coefficients from soft_exp2_fit.py); n is added to the exponent field.  x is
-// clamped at -127, where the result is below the normal range (the hardware path flushes it).
+// error 8.6e-5; coefficients from soft_exp2_fit.py); n is added to the exponent field.  Below
+// -126 the result is 0, as the flushing hardware path gives (masked scores are -inf).
 constexpr float kExp2C1 = 0.69511676f, kExp2C2 = 0.227645f, kExp2C3 = 0.07706704f;
 __device__ __forceinline__ float2 soft_exp2x2(float2 x) {
   constexpr float kRound = 12582912.0f;   // 1.5 * 2^23: x + kRound, rounded down, is kRound + n
-  x.x = fmaxf(x.x, -127.0f);
+  const bool lo_x = x.x < -126.0f, lo_y = x.y < -126.0f;
+  x.x = fmaxf(x.x, -127.0f);   // keeps n in range (and -inf finite) before the result is dropped
   x.y = fmaxf(x.y, -127.0f);
   const float2 rr = make_float2(kRound, kRound);
   const float2 t = ptx::fadd2_rm(x, rr);
@@ -583,6 +584,8 @@ __device__ __forceinline__ float2 soft_exp2x2(float2 x) {
   const int bias = __float_as_int(kRound);
   y.x = __int_as_float(__float_as_int(y.x) + ((__float_as_int(t.x) - bias) << 23));
   y.y = __int_as_float(__float_as_int(y.y) + ((__float_as_int(t.y) - bias) << 23));
+  if (lo_x) y.x = 0.0f;
+  if (lo_y) y.y = 0.0f;
   return y;
 }
 

@@ -33,16 +33,18 @@ def fma32(a, b, c):
 
 def soft_exp2_fp32(x):
     """The kernel's algorithm in fp32: clamp at -127, n = floor(x), f = x - n (exact), Horner in
-    single-rounding FMAs, n added to the exponent field."""
+    single-rounding FMAs, n added to the exponent field; 0 below -126."""
     c1, c2, c3 = kernel_coefficients()
-    x = np.maximum(x.astype(np.float32), np.float32(-127.0))
+    x = x.astype(np.float32)
+    low = x < np.float32(-126.0)
+    x = np.maximum(x, np.float32(-127.0))
     n = np.floor(x)
     f = (x - n).astype(np.float32)
     y = fma32(np.full_like(f, c3), f, np.full_like(f, c2))
     y = fma32(y, f, np.full_like(f, c1))
     y = fma32(y, f, np.ones_like(f))
     bits = y.view(np.int32) + (n.astype(np.int32) << 23)
-    return bits.view(np.float32)
+    return np.where(low, np.float32(0.0), bits.view(np.float32))
 
 
 def test_kernel_coefficients_are_the_minimax_fit():
@@ -77,7 +79,8 @@ def test_software_exp2_against_fp64():
     assert np.array_equal(soft_exp2_fp32(xi), np.exp2(xi.astype(np.float64)).astype(np.float32))
 
 
-def test_software_exp2_clamps_below_the_normal_range():
-    # below -127 the clamp gives a value under the smallest normal (the hardware path gives 0)
-    v = soft_exp2_fp32(np.array([-127.0, -150.0, -1e30], dtype=np.float32))
-    assert np.all(v < np.float32(2.0 ** -126))
+def test_software_exp2_is_zero_below_the_normal_range():
+    # as the flushing hardware exp2: masked scores (-inf) and anything below -126 give exactly 0
+    v = soft_exp2_fp32(np.array([-126.5, -127.0, -150.0, -1e30, -np.inf], dtype=np.float32))
+    assert np.all(v == 0.0)
+    assert soft_exp2_fp32(np.array([-126.0], dtype=np.float32))[0] == np.float32(2.0 ** -126)
