@@ -273,6 +273,9 @@ def run_ours(args):
                                                         seed=w.seeds[0] + 100)[0]).to(dev)
             extra = (dout, torch.empty_like(d[0]), torch.empty_like(d[1]), torch.empty_like(d[2]),
                      torch.empty(w.B, w.H, w.Sq, dtype=torch.float32, device=dev))
+        if not backward:
+            # attn_fwd_ws's workspace (None where the schedule runs whole items only)
+            extra = attn.workspace_for(d[0], d[1], causal=causal, layout=layout, soft_exp2=soft)
         shapes.append((w, (qb, kb, vb), host, d, o, lse, extra))
     flops = flop_factor * sum(w.flops for w, *_ in shapes)
     stream = torch.cuda.current_stream()
@@ -283,7 +286,7 @@ def run_ours(args):
     def one(w, d, o, lse, extra):
         if not backward:
             attn.fwd_into(d[0], d[1], d[2], o, lse, w.scale, causal=causal, layout=layout,
-                          soft_exp2=soft)
+                          soft_exp2=soft, workspace=extra)
             return
         dout, dq, dk, dv, delta = extra
         rc = lib.attn_bwd(d[0].data_ptr(), d[1].data_ptr(), d[2].data_ptr(), o.data_ptr(),

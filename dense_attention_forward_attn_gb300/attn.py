@@ -41,9 +41,10 @@ class _Plan(ctypes.Structure):
                 ("smem_bytes", ctypes.c_int), ("tmem_cols", ctypes.c_int)]
 
 
-EXPORTS = ("attn_fwd", "attn_fwd_ex", "attn_fwd_host", "attn_fwd_host_workspace",
-           "attn_fwd_host_chunking", "attn_bwd", "attn_bwd_noalloc", "attn_status_string",
-           "attn_fwd_plan", "attn_fwd_work_item", "attn_fwd_schedule", "attn_device_status")
+EXPORTS = ("attn_fwd", "attn_fwd_ex", "attn_fwd_ws", "attn_fwd_workspace", "attn_fwd_segment",
+           "attn_fwd_host", "attn_fwd_host_workspace", "attn_fwd_host_chunking", "attn_bwd",
+           "attn_bwd_noalloc", "attn_status_string", "attn_fwd_plan", "attn_fwd_work_item",
+           "attn_fwd_schedule", "attn_device_status")
 
 
 def lib_path() -> str:
@@ -57,6 +58,13 @@ def _bind(lib):
     lib.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp]
     lib.attn_fwd_ex.restype = i32
     sz = ctypes.c_size_t
+    lib.attn_fwd_ws.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
+    lib.attn_fwd_ws.restype = i32
+    lib.attn_fwd_workspace.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
+    lib.attn_fwd_workspace.restype = i32
+    ipp = ctypes.POINTER(i32)
+    lib.attn_fwd_segment.argtypes = [i32, i32, i32, i64, i32, i32, ipp, ipp, ipp, ipp, ipp]
+    lib.attn_fwd_segment.restype = i32
     lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
     lib.attn_fwd_host.restype = i32
     lib.attn_fwd_host_workspace.argtypes = [i32, i32, i32, i32, i32, i32, ctypes.POINTER(sz)]
@@ -136,6 +144,37 @@ def schedule(cta: int, rnd: int, grid: int, work_items: int, causal: bool = Fals
     return int(library().attn_fwd_schedule(cta, rnd, grid, work_items, _flags(causal)))
 
 
+def segment(cta: int, rnd: int, grid: int, work_items: int, kv_tiles: int, causal: bool = False):
+    """The turn `rnd` of CTA `cta` under attn_fwd_ws's schedule: None when the CTA has no more,
+    else (item, first KV tile, KV tile count or -1 for the whole item, split slot or -1, part)."""
+    out = [ctypes.c_int() for _ in range(5)]
+    rc = library().attn_fwd_segment(cta, rnd, grid, work_items, kv_tiles, _flags(causal),
+                                    *(ctypes.byref(x) for x in out))
+    if rc < 0:
+        raise AttnError(rc, "attn_fwd_segment")
+    return tuple(x.value for x in out) if rc == 1 else None
+
+
+def workspace_bytes(B: int, H: int, Sq: int, Sk: int, D: int = 128, causal: bool = False,
+                    layout: str = "bhsd", soft_exp2: bool = False) -> int:
+    """Workspace attn_fwd_ws needs for this problem on the current device (0: none)."""
+    n = ctypes.c_size_t(0)
+    rc = library().attn_fwd_workspace(B, H, Sq, Sk, D, _flags(causal, layout, soft_exp2),
+                                      ctypes.byref(n))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_workspace")
+    return int(n.value)
+
+
+def workspace_for(q, k, causal: bool = False, layout: str = "bhsd", soft_exp2: bool = False):
+    """A device workspace for fwd_into(..., workspace=...) with these q/k, or None if the call
+    does not need one.  Allocated from PyTorch's caching allocator on q's device."""
+    import torch
+    B, H, Sq, Sk, D = _dims(q, k, layout)
+    n = workspace_bytes(B, H, Sq, Sk, D, causal, layout, soft_exp2)
+    return torch.empty(n, dtype=torch.uint8, device=q.device) if n else None
+
+
 def host_chunking(B: int, H: int, Sq: int, Sk: int, num_sms: int, causal: bool = False,
                   layout: str = "bhsd"):
     """(units per chunk, chunks) of the host-buffer forward; units are heads ([B,H,S,D]) or
@@ -174,11 +213,14 @@ def _dims(q, k, layout):
 
 
 def fwd_into(q, k, v, o, lse=None, scale: float | None = None, stream=None,
-             causal: bool = False, layout: str = "bhsd", soft_exp2: bool = False) -> None:
+             causal: bool = False, layout: str = "bhsd", soft_exp2: bool = False,
+             workspace=None) -> None:
     """Device tensors only: write softmax(scale q k^T) v into `o` (and LSE into `lse`).
 
     layout "bhsd": q/o [B,H,Sq,D], k/v [B,H,Sk,D]; "bshd": q/o [B,Sq,H,D], k/v [B,Sk,H,D].
     lse is [B,H,Sq] either way.  soft_exp2: ATTN_FLAG_SOFT_EXP2 (off by default).
+    workspace: None calls attn_fwd_ex (whole work items only); a uint8 CUDA tensor (from
+    workspace_for) calls attn_fwd_ws, which evens out the persistent grid's last rounds.
     """
     import torch
     flags = _flags(causal, layout, soft_exp2)
@@ -195,9 +237,17 @@ def fwd_into(q, k, v, o, lse=None, scale: float | None = None, stream=None,
         scale = 1.0 / math.sqrt(D)
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
-    rc = library().attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                               lse.data_ptr() if lse is not None else None, B, H, Sq, Sk, D,
-                               float(scale), flags, stream)
+    lse_ptr = lse.data_ptr() if lse is not None else None
+    if workspace is None:
+        rc = library().attn_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse_ptr,
+                                   B, H, Sq, Sk, D, float(scale), flags, stream)
+    else:
+        if (not isinstance(workspace, torch.Tensor) or not workspace.is_cuda
+                or workspace.device != q.device or not workspace.is_contiguous()):
+            raise ValueError("workspace must be a contiguous CUDA tensor on q's device")
+        rc = library().attn_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse_ptr,
+                                   B, H, Sq, Sk, D, float(scale), flags, workspace.data_ptr(),
+                                   workspace.numel() * workspace.element_size(), stream)
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
 
@@ -207,7 +257,8 @@ def fwd(q, k, v, scale: float | None = None, return_lse: bool = True, causal: bo
     """Attention forward.  q [B,H,Sq,D], k/v [B,H,Sk,D] (or [B,S,H,D] with layout="bshd"),
     BF16 contiguous.  Returns (o in q's layout, lse [B,H,Sq] or None).
 
-    CUDA tensors: runs on the current stream, returns (o, lse) on the device.
+    CUDA tensors: runs on the current stream through attn_fwd_ws (with a workspace from
+    PyTorch's caching allocator when the schedule needs one), returns (o, lse) on the device.
     CPU tensors: attn_fwd_host -- the library copies the inputs to the current
     CUDA device in chunks (pinned host memory, pinned here first if needed),
     overlapping the copies with the kernel, copies O and LSE back into pinned
@@ -221,7 +272,9 @@ def fwd(q, k, v, scale: float | None = None, return_lse: bool = True, causal: bo
         return _fwd_host(q, k, v, B, H, Sq, Sk, D, scale, return_lse, causal, layout, soft_exp2)
     o = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device) if return_lse else None
-    fwd_into(q, k, v, o, lse, scale, causal=causal, layout=layout, soft_exp2=soft_exp2)
+    ws = workspace_for(q, k, causal, layout, soft_exp2)
+    fwd_into(q, k, v, o, lse, scale, causal=causal, layout=layout, soft_exp2=soft_exp2,
+             workspace=ws)   # None: the call has no split rounds, attn_fwd_ex
     return o, lse
 
 

@@ -7,7 +7,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
+#include <random>
 
 #include "../../include/attn_fwd.h"
 #include "attn_fwd_kernel.cuh"
@@ -56,17 +58,19 @@ int device_info(int dev, DeviceInfo* out) {
     return fa.numRegs == want;
   };
   if (!d.attr_set) {
-    if (cudaFuncSetAttribute(attn::attn_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(attn::kSmemBytes)) != cudaSuccess ||
-        cudaFuncSetAttribute(attn::attn_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(attn::kSmemBytes)) != cudaSuccess) {
-      cudaGetLastError();
-      return ATTN_ERR_CUDA;
-    }
-    if (!regs_are(reinterpret_cast<const void*>(attn::attn_fwd_kernel<false>), 65536 / attn::kThreads) ||
-        !regs_are(reinterpret_cast<const void*>(attn::attn_fwd_kernel<true>), 65536 / attn::kThreads)) {
-      cudaGetLastError();
-      return ATTN_ERR_UNSUPPORTED;
+    const void* fwd_kernels[] = {reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false>),
+                                 reinterpret_cast<const void*>(attn::attn_fwd_kernel<true, false>),
+                                 reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true>)};
+    for (const void* fn : fwd_kernels) {
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(attn::kSmemBytes)) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+      }
+      if (!regs_are(fn, 65536 / attn::kThreads)) {
+        cudaGetLastError();
+        return ATTN_ERR_UNSUPPORTED;
+      }
     }
     d.attr_set = true;
   }
@@ -147,6 +151,59 @@ int check_shape(int B, int H, int Sq, int Sk, int D) {
   return ATTN_OK;
 }
 
+// The split schedule of attn_fwd_ws for a problem of `items` work items of `kv_tiles` KV tiles
+// each on `grid` persistent CTAs.  Whole rounds run as before; when the last round would be
+// partly idle, the last two rounds' items (between grid and 2*grid of them) are instead cut by
+// KV range so every CTA gets the same number of (item, KV tile) units.  Used only where that
+// shortens the longest CTA by at least kSplitMinGainTiles KV tiles: measured on GB300, every
+// extra segment of a CTA costs about 2 us (1.5 KV-tile iterations) of pipeline fill and drain and
+// the combining epilogue about 3 us, so at S=4K with 16 heads (8 tiles of gain) the split ran
+// 1-2% slower, while at S=8K/16K/12K (17/33/40 tiles) it ran 1%/2.7%/3.8% faster.
+// Dense, non-causal, exp2 on MUFU only.
+struct SplitPlan {
+  bool on = false;
+  int sk_item0 = 0, sk_items = 0;
+  size_t off_flag = 0, off_l = 0, off_o = 0, bytes = 0;
+};
+
+SplitPlan split_plan(int64_t items, int grid, int kv_tiles, int flags) {
+  SplitPlan sp;
+  if (flags & (ATTN_FLAG_CAUSAL | ATTN_FLAG_SOFT_EXP2 | ATTN_FLAG_TEST_WITHHOLD)) return sp;
+  if (grid < 2 || items <= grid || items % grid == 0 || kv_tiles < 2) return sp;
+  const int64_t sk_item0 = (items / grid - 1) * grid;
+  const int64_t sk_items = items - sk_item0;   // in (grid, 2 grid)
+  const int64_t units = sk_items * kv_tiles;
+  if (units * grid > INT32_MAX) return sp;   // the kernel's unit arithmetic is 32-bit
+  const int64_t longest = (units + grid - 1) / grid;
+  constexpr int64_t kSplitMinGainTiles = 12;
+  if (2 * static_cast<int64_t>(kv_tiles) - longest < kSplitMinGainTiles) return sp;
+  sp.on = true;
+  sp.sk_item0 = static_cast<int>(sk_item0);
+  sp.sk_items = static_cast<int>(sk_items);
+  const size_t slots = static_cast<size_t>(grid - 1);
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  sp.off_flag = 0;
+  sp.off_l = up(slots * 2 * 4 * sizeof(unsigned long long));
+  sp.off_o = sp.off_l + up(slots * 2 * 2 * attn::kBlockM * sizeof(float));
+  sp.bytes = sp.off_o + slots * 2 * 2 * attn::kBlockM * attn::kHeadDim * sizeof(float);
+  return sp;
+}
+
+// Per-call sequence numbers for the split schedule's flags: a random 32-bit salt per process in
+// the high half, so numbers left in a workspace by another process or an earlier call differ.
+unsigned long long next_seq() {
+  static std::atomic<unsigned long long> counter{0};
+  static const unsigned long long salt = [] {
+    std::random_device rd;
+    return (static_cast<unsigned long long>(rd()) | 1ull) << 32;
+  }();
+  return salt + counter.fetch_add(1, std::memory_order_relaxed);
+}
+
+int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int Sq, int Sk, int D, float scale, int flags, void* workspace,
+               size_t workspace_bytes, bool use_ws, void* stream);
+
 }  // namespace
 
 extern "C" {
@@ -225,6 +282,75 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 
 int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                 int Sq, int Sk, int D, float scale, int flags, void* stream) {
+  return launch_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale, flags, nullptr, 0, false, stream);
+}
+
+int attn_fwd_workspace(int B, int H, int Sq, int Sk, int D, int flags, size_t* bytes) {
+  if (bytes == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (flags & ~ATTN_FLAGS_ALL) return ATTN_ERR_INVALID_ARG;
+  const int rc = check_shape(B, H, Sq, Sk, D);
+  if (rc != ATTN_OK) return rc;
+  *bytes = 0;
+  const int64_t bh = static_cast<int64_t>(B) * H;
+  if (bh == 0 || Sq == 0) return ATTN_OK;
+  int dev = 0, num_sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  const int64_t items = bh * ((ceil_div(Sq, attn::kBlockM) + 1) / 2);
+  const int grid = static_cast<int>(items < num_sms ? items : num_sms);
+  *bytes = split_plan(items, grid, ceil_div(Sk, attn::kBlockN), flags).bytes;
+  return ATTN_OK;
+}
+
+int attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int Sq, int Sk, int D, float scale, int flags, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  return launch_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale, flags, workspace, workspace_bytes,
+                    true, stream);
+}
+
+int attn_fwd_segment(int cta, int round, int grid, int64_t work_items, int kv_tiles, int flags,
+                     int* item, int* kv_tile0, int* kv_count, int* slot, int* part) {
+  if (!item || !kv_tile0 || !kv_count || !slot || !part) return ATTN_ERR_INVALID_ARG;
+  if (cta < 0 || round < 0 || grid <= 0 || cta >= grid || work_items < 0 ||
+      work_items > INT32_MAX || kv_tiles <= 0 || (flags & ~ATTN_FLAGS_ALL))
+    return ATTN_ERR_INVALID_ARG;
+  const SplitPlan sp = split_plan(work_items, grid, kv_tiles, flags);
+  *slot = -1;
+  *part = 0;
+  if (!sp.on || static_cast<int64_t>(round) * grid < sp.sk_item0) {
+    const int it = attn::item_of(round, cta, grid, static_cast<int>(work_items),
+                                 (flags & ATTN_FLAG_CAUSAL) != 0);
+    if (it < 0) return 0;
+    *item = it;
+    *kv_tile0 = 0;
+    *kv_count = -1;   // the whole item (its KV tiles per Q tile: attn_fwd_work_item)
+    return 1;
+  }
+  int il, j0, cnt;
+  if (!attn::split_segment(round - sp.sk_item0 / grid, cta, grid, sp.sk_items, kv_tiles, il, j0,
+                           cnt))
+    return 0;
+  *item = sp.sk_item0 + il;
+  *kv_tile0 = j0;
+  *kv_count = cnt;
+  if (cnt < kv_tiles) {
+    *part = j0 > 0 ? 1 : 0;
+    *slot = j0 > 0 ? cta - 1 : cta;
+  }
+  return 1;
+}
+
+}  // extern "C"
+
+namespace {
+
+int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int Sq, int Sk, int D, float scale, int flags, void* workspace,
+               size_t workspace_bytes, bool use_ws, void* stream) {
   if (flags & ~ATTN_FLAGS_ALL) return ATTN_ERR_INVALID_ARG;
   int rc = check_shape(B, H, Sq, Sk, D);
   if (rc != ATTN_OK) return rc;
@@ -279,16 +405,47 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   p.test_withhold = (flags & ATTN_FLAG_TEST_WITHHOLD) ? 1 : 0;
   const int grid = p.num_items < info.num_sms ? p.num_items : info.num_sms;
+  p.sk_item0 = p.num_items;
+  p.sk_items = 0;
+  p.ws_o = p.ws_l = nullptr;
+  p.ws_flag = nullptr;
+  p.seq = 0;
+  const SplitPlan sp = use_ws ? split_plan(p.num_items, grid, p.kv_tiles, flags) : SplitPlan();
+  if (sp.on) {
+    if (workspace == nullptr || workspace_bytes < sp.bytes ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+      return ATTN_ERR_INVALID_ARG;
+    const size_t nw = sp.bytes;
+    if (overlaps(workspace, nw, q, nq) || overlaps(workspace, nw, k, nk) ||
+        overlaps(workspace, nw, v, nk) || overlaps(workspace, nw, o, nq) ||
+        overlaps(workspace, nw, lse, nl))
+      return ATTN_ERR_INVALID_ARG;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.sk_item0 = sp.sk_item0;
+    p.sk_items = sp.sk_items;
+    p.ws_flag = reinterpret_cast<unsigned long long*>(ws + sp.off_flag);
+    p.ws_l = reinterpret_cast<float*>(ws + sp.off_l);
+    p.ws_o = reinterpret_cast<float*>(ws + sp.off_o);
+    p.seq = next_seq();
+  }
 
-  if (flags & ATTN_FLAG_SOFT_EXP2)
-    attn::attn_fwd_kernel<true><<<grid, attn::kThreads, attn::kSmemBytes,
-                                  static_cast<cudaStream_t>(stream)>>>(tm_q, tm_k, tm_v, p);
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (sp.on)
+    attn::attn_fwd_kernel<false, true><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tm_q, tm_k,
+                                                                                      tm_v, p);
+  else if (flags & ATTN_FLAG_SOFT_EXP2)
+    attn::attn_fwd_kernel<true, false><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tm_q, tm_k,
+                                                                                      tm_v, p);
   else
-    attn::attn_fwd_kernel<false><<<grid, attn::kThreads, attn::kSmemBytes,
-                                   static_cast<cudaStream_t>(stream)>>>(tm_q, tm_k, tm_v, p);
+    attn::attn_fwd_kernel<false, false><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tm_q, tm_k,
+                                                                                       tm_v, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 int attn_device_status(unsigned int* word, int clear) {
   if (word == nullptr) return ATTN_ERR_INVALID_ARG;

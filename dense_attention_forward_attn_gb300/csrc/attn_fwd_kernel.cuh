@@ -122,6 +122,7 @@ struct alignas(8) SmemCtl {
   uint64_t drain;
   uint32_t tmem_base;
   volatile int abort_flag;
+  int sk_range[2];              // split schedule: this CTA's (item, KV tile) units [a, b)
   float alpha[2][2][kBlockM];   // [stage][tile parity][row]
 };
 
@@ -147,6 +148,16 @@ struct Params {
   float scale_log2; // scale * log2(e)
   int test_withhold;  // test hook: CTA 0's TMA warp never loads its first K tile, so the MMA
                       // warp's bounded wait on it expires (exercises the failure path)
+  // Split schedule (the kernel's kSplit instantiation): items before sk_item0 (a multiple of the
+  // grid) run whole by static stride; the remaining sk_items are cut by KV range so that every
+  // CTA gets the same number of (item, KV tile) units.  An item whose KV range is shared by two
+  // CTAs leaves a partial result of each part in the workspace; the second to finish combines.
+  int sk_item0;
+  int sk_items;
+  float* ws_o;                  // [slot][part][stage][32 chunks][128 rows][4] fp32: O / l
+  float* ws_l;                  // [slot][part][stage][128 rows] fp32: kept max + log2 l
+  unsigned long long* ws_flag;  // [slot][stage][warp]: seq of the call whose part arrived
+  unsigned long long seq;       // unique per call: flags from earlier calls never match it
 };
 
 struct WorkItem {
@@ -188,6 +199,71 @@ __device__ __forceinline__ WorkItem decode_item(int item, const Params& p) {
 __host__ __device__ inline int item_of(int round, int cta, int grid, int num_items, bool causal) {
   const int k = round * grid + ((causal && (round & 1)) ? grid - 1 - cta : cta);
   return k < num_items ? k : -1;
+}
+
+// Split schedule: CTA `cta` owns units [U*cta/grid, U*(cta+1)/grid) of the U = sk_items * n
+// (item, KV tile) units of the split part, item-major.  Every CTA owns at least n units
+// (sk_items > grid), so an item is shared by at most two CTAs: the head part (KV tiles [0, x))
+// ends the range of CTA s, the tail part (KV tiles [x, n)) starts the range of CTA s + 1, and s
+// is the split's slot.  Segment k of a CTA's range: item (local to the split part), first KV
+// tile and KV tile count; false when the range has fewer segments.
+// The host enables the split only where U * grid fits in 31 bits.
+__host__ __device__ inline int split_range_begin(int cta, int grid, int sk_items, int n) {
+  return static_cast<int>(static_cast<int64_t>(sk_items) * n * cta / grid);
+}
+// Segment k of the range [a, b) (from split_range_begin of this CTA and the next).
+__host__ __device__ inline bool split_segment_of_range(int k, int a, int b, int n, int& item_local,
+                                                       int& j0, int& cnt) {
+  const int it = a / n + k;
+  const int start = k == 0 ? a : it * n;
+  if (start >= b) return false;
+  const int end = b < (it + 1) * n ? b : (it + 1) * n;
+  item_local = it;
+  j0 = start - it * n;
+  cnt = end - start;
+  return true;
+}
+__host__ __device__ inline bool split_segment(int k, int cta, int grid, int sk_items, int n,
+                                              int& item_local, int& j0, int& cnt) {
+  return split_segment_of_range(k, split_range_begin(cta, grid, sk_items, n),
+                                split_range_begin(cta + 1, grid, sk_items, n), n, item_local, j0,
+                                cnt);
+}
+
+// One turn of a persistent CTA: a whole work item, or one part of an item split by KV range.
+struct Seg {
+  WorkItem w;   // n[q]: KV tiles of this segment for Q tile qt0 + q
+  int j0;       // first KV tile of the segment
+  int slot;     // -1: the whole item; else the index of the split
+  int part;     // 0: the item's KV tiles [0, x); 1: its KV tiles [x, n)
+};
+
+// sk_range: this CTA's unit range [a, b) of the split part (set once per CTA, in shared memory).
+template <bool kSplit>
+__device__ __forceinline__ bool seg_of(int r, const Params& p, const int* sk_range, Seg& s) {
+  const int cta = static_cast<int>(blockIdx.x), grid = static_cast<int>(gridDim.x);
+  s.j0 = 0;
+  s.slot = -1;
+  s.part = 0;
+  if (!kSplit || r * grid < p.sk_item0) {
+    const int item = item_of(r, cta, grid, p.num_items, p.causal != 0);
+    if (item < 0) return false;
+    s.w = decode_item(item, p);
+    return true;
+  }
+  int il, j0, cnt;
+  if (!split_segment_of_range(r - p.sk_item0 / grid, sk_range[0], sk_range[1], p.kv_tiles, il, j0,
+                              cnt))
+    return false;
+  s.w = decode_item(p.sk_item0 + il, p);
+  s.w.n[0] = cnt;
+  if (s.w.n[1] > 0) s.w.n[1] = cnt;
+  s.j0 = j0;
+  if (cnt < p.kv_tiles) {
+    s.part = j0 > 0 ? 1 : 0;
+    s.slot = j0 > 0 ? cta - 1 : cta;
+  }
+  return true;
 }
 
 // tcgen05 shared-memory matrix descriptor, 128-byte swizzle.
@@ -291,6 +367,7 @@ struct Ctx {
 };
 
 // ------------------------------------------------------------------ TMA warp
+template <bool kSplit>
 __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const CUtensorMap* tm_q,
                                           const CUtensorMap* tm_k, const CUtensorMap* tm_v) {
   SmemCtl* ctl = c.ctl;
@@ -358,28 +435,29 @@ __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const C
   };
 
   for (int r = 0; ok; ++r) {
-    const int item = item_of(r, blockIdx.x, gridDim.x, p.num_items, p.causal != 0);
-    if (item < 0) break;
-    const WorkItem w = decode_item(item, p);
+    Seg sg;
+    if (!seg_of<kSplit>(r, p, ctl->sk_range, sg)) break;
+    const WorkItem& w = sg.w;
     const int row0 = w.qt0 * kBlockM;
     const int ntiles = w.n[1] > 0 ? w.n[1] : w.n[0];   // n[1] >= n[0] whenever it is non-zero
+    const int kv0 = sg.j0 * kBlockN;                    // first key row of the segment
 #if ATTN_L2_PREFETCH > 0
     for (int j = 0; j < ATTN_L2_PREFETCH && j < ntiles; ++j) {
-      prefetch(tm_k, w.bh, j * kBlockN);
-      prefetch(tm_v, w.bh, j * kBlockN);
+      prefetch(tm_k, w.bh, kv0 + j * kBlockN);
+      prefetch(tm_v, w.bh, kv0 + j * kBlockN);
     }
 #endif
-    ok = load_q(0, w.bh, row0) && load_kv(tm_k, w.bh, 0);
+    ok = load_q(0, w.bh, row0) && load_kv(tm_k, w.bh, kv0);
     if (ok && w.n[1] > 0) ok = load_q(1, w.bh, row0 + kBlockM);
-    if (ok) ok = load_kv(tm_v, w.bh, 0);
+    if (ok) ok = load_kv(tm_v, w.bh, kv0);
     for (int j = 1; ok && j < ntiles; ++j) {
 #if ATTN_L2_PREFETCH > 0
       if (j + ATTN_L2_PREFETCH - 1 < ntiles) {
-        prefetch(tm_k, w.bh, (j + ATTN_L2_PREFETCH - 1) * kBlockN);
-        prefetch(tm_v, w.bh, (j + ATTN_L2_PREFETCH - 1) * kBlockN);
+        prefetch(tm_k, w.bh, kv0 + (j + ATTN_L2_PREFETCH - 1) * kBlockN);
+        prefetch(tm_v, w.bh, kv0 + (j + ATTN_L2_PREFETCH - 1) * kBlockN);
       }
 #endif
-      ok = load_kv(tm_k, w.bh, j * kBlockN) && load_kv(tm_v, w.bh, j * kBlockN);
+      ok = load_kv(tm_k, w.bh, kv0 + j * kBlockN) && load_kv(tm_v, w.bh, kv0 + j * kBlockN);
     }
   }
   if (!ok) {
@@ -418,6 +496,7 @@ __device__ __forceinline__ void issue_pv(const Ctx& c, int vslot, bool overwrite
   }
 }
 
+template <bool kSplit>
 __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
   SmemCtl* ctl = c.ctl;
   const bool leader = ptx::elect_one();
@@ -475,17 +554,17 @@ __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
   // its last P V; a stage that ends earlier (stage 0 of a causal pair) defers it to the end of
   // the item, after the last token of the item has been consumed.
   int r = 0;
-  int item = item_of(0, blockIdx.x, gridDim.x, p.num_items, p.causal != 0);
-  if (item >= 0) {
-    WorkItem w = decode_item(item, p);
+  Seg sg;
+  if (seg_of<kSplit>(0, p, ctl->sk_range, sg)) {
+    WorkItem w = sg.w;
     int kslot;
     ok = next_kv(kslot) && qk(0, kslot, true, w.n[0] == 1, w.n[1] == 0);
     if (ok && w.n[1] > 0) ok = qk(1, kslot, true, w.n[1] == 1, true);
     while (ok) {
       const int ntiles = w.n[1] > 0 ? w.n[1] : w.n[0];
-      const int nitem = item_of(r + 1, blockIdx.x, gridDim.x, p.num_items, p.causal != 0);
-      const bool has_next = nitem >= 0;
-      const WorkItem nw = has_next ? decode_item(nitem, p) : w;
+      Seg nsg;
+      const bool has_next = seg_of<kSplit>(r + 1, p, ctl->sk_range, nsg);
+      const WorkItem nw = has_next ? nsg.w : w;
       int next_kslot = -1;
       // First Q K of stage q for the next item (its K_0 is acquired once for both stages).
       auto issue_next = [&](int q) -> bool {
@@ -536,7 +615,6 @@ __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
       if (!next0_done && !(ok = issue_next(0))) break;
       if (!(ok = issue_next(1))) break;
       if (!has_next) break;
-      item = nitem;
       w = nw;
       ++r;
     }
@@ -679,7 +757,111 @@ __device__ __forceinline__ void epilogue_store(const Params& p, int q, const Wor
     p.lse[static_cast<size_t>(w.bh) * p.sq + grow] = (m + log2f(l)) * 0.69314718055994530942f;
 }
 
-template <bool kSoftExp2>
+// Item epilogue of stage q for one part of an item split between two CTAs (this warp's 32 rows).
+// The warp first looks at its flag: if the partner part's warp has already left the call's
+// sequence number there, its O / l (fp32) and base-2 LSE are in the workspace and this warp
+// combines at once.  Otherwise it writes its own part there and swaps the sequence number into
+// the flag; if that swap returns the number, the partner wrote in the meantime and this warp
+// combines, else the partner will.  Exactly one of the two warps combines, and neither waits.
+// The combination is O = w0 O0/l0 + w1 O1/l1 with w_i = 2^(L_i - L), L = log2(2^L0 + 2^L1),
+// each product and the sum rounded separately, so it is the same whichever warp computes it.
+// Not inlined: it runs at most twice per CTA, and inlined into the softmax role it slowed the
+// whole-item rounds by 0.5-1% (larger loop code).
+__device__ __noinline__ bool epilogue_split(const Ctx& c, const Params& p, int q, const Seg& sg,
+                                               int row, float m, float l, uint32_t o_parity) {
+  if (!c.wait(c.ctl->o_full[q], o_parity, kStatusTimeoutSoftmax)) return false;
+  ptx::tc_fence_after();
+  const uint32_t taddr_o = c.tmem + ((32u * (c.warp & 3u)) << 16) + col_o(q);
+  const float inv_l = 1.0f / l;
+  const float L_own = m + log2f(l);
+  constexpr size_t kPartFloats = static_cast<size_t>(kBlockM) * kHeadDim;
+  const size_t own = (static_cast<size_t>(sg.slot) * 2 + sg.part) * 2 + q;   // [slot][part][stage]
+  const size_t oth = (static_cast<size_t>(sg.slot) * 2 + (1 - sg.part)) * 2 + q;
+  unsigned long long* flag = p.ws_flag + (static_cast<size_t>(sg.slot) * 2 + q) * 4 + (c.warp & 3u);
+  unsigned long long f = 0;
+  if (c.lane == 0) f = ptx::ld_acquire_u64(flag);
+  f = __shfl_sync(0xffffffffu, f, 0);
+  if (f != p.seq) {
+    float* dst = p.ws_o + own * kPartFloats + row * 4;   // chunk i (4 columns) at + i * 128 * 4
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      uint32_t r[32];
+      ptx::tmem_ld_32x32b_x32(taddr_o + 32 * cc, r);
+      ptx::tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        ptx::st_global_v4(dst + (cc * 8 + i) * kBlockM * 4,
+                          __float_as_uint(__uint_as_float(r[4 * i]) * inv_l),
+                          __float_as_uint(__uint_as_float(r[4 * i + 1]) * inv_l),
+                          __float_as_uint(__uint_as_float(r[4 * i + 2]) * inv_l),
+                          __float_as_uint(__uint_as_float(r[4 * i + 3]) * inv_l));
+    }
+    p.ws_l[own * kBlockM + row] = L_own;
+    __threadfence();
+    __syncwarp();
+    if (c.lane == 0) {
+      f = atomicExch(flag, p.seq);
+      __threadfence();
+    }
+    f = __shfl_sync(0xffffffffu, f, 0);
+    if (f != p.seq) {   // the partner combines
+      ptx::tc_fence_before();
+      return true;
+    }
+  }
+  __threadfence();
+  // Combine: this part from TMEM (O / l recomputed exactly as stored), the other from the workspace.
+  const float L_oth = __ldcg(p.ws_l + oth * kBlockM + row);
+  const float L0 = sg.part == 0 ? L_own : L_oth, L1 = sg.part == 0 ? L_oth : L_own;
+  const float L = fmaxf(L0, L1);
+  const float e0 = ptx::ex2_ftz(L0 - L), e1 = ptx::ex2_ftz(L1 - L);
+  const float sum = e0 + e1;
+  const float w0 = e0 / sum, w1 = e1 / sum;
+  const float w_own = sg.part == 0 ? w0 : w1, w_oth = sg.part == 0 ? w1 : w0;
+  const float4* src = reinterpret_cast<const float4*>(p.ws_o + oth * kPartFloats) + row;
+  const int grow = (sg.w.qt0 + q) * kBlockM + row;
+  const bool store = grow < p.sq;
+  const int b = sg.w.bh / p.heads, h = sg.w.bh - b * p.heads;
+  uint8_t* out = static_cast<uint8_t*>(p.o) +
+                 (b * p.o_batch_stride + h * p.o_head_stride + grow * p.o_row_stride) * 2;
+  float4 nxt[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) nxt[i] = __ldcg(src + i * kBlockM);
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {   // 32 columns per step, the next step's loads in flight
+    float4 cur[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
+    if (cc < 3) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) nxt[i] = __ldcg(src + ((cc + 1) * 8 + i) * kBlockM);
+    }
+    uint32_t r[32];
+    ptx::tmem_ld_32x32b_x32(taddr_o + 32 * cc, r);
+    ptx::tmem_wait_ld();
+    auto mix = [&](int k, float oth_v) {
+      const float own_v = __uint_as_float(r[k]) * inv_l;
+      return __fadd_rn(__fmul_rn(own_v, w_own), __fmul_rn(oth_v, w_oth));
+    };
+    if (store) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {   // 8 columns = 16 bytes of BF16
+        const float4 x = cur[2 * i], y = cur[2 * i + 1];
+        ptx::st_global_v4(out + 64 * cc + 16 * i,
+                          ptx::pack_bf16x2(mix(8 * i, x.x), mix(8 * i + 1, x.y)),
+                          ptx::pack_bf16x2(mix(8 * i + 2, x.z), mix(8 * i + 3, x.w)),
+                          ptx::pack_bf16x2(mix(8 * i + 4, y.x), mix(8 * i + 5, y.y)),
+                          ptx::pack_bf16x2(mix(8 * i + 6, y.z), mix(8 * i + 7, y.w)));
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  if (store && p.lse != nullptr)
+    p.lse[static_cast<size_t>(sg.w.bh) * p.sq + grow] = (L + log2f(sum)) * 0.69314718055994530942f;
+  return true;
+}
+
+template <bool kSoftExp2, bool kSplit>
 __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int q) {
   SmemCtl* ctl = c.ctl;
   const uint32_t row_base = 32u * (c.warp & 3u);
@@ -693,13 +875,13 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
   uint32_t tphase = 0;
   uint32_t o_parity = 0;     // o_full phase of the previous item
   bool have_prev = false;    // an item whose epilogue is still to do
-  WorkItem wp;
+  Seg sp;
   float m_prev = 0.f, l_prev = 1.f;
 
   for (int r = 0;; ++r) {
-    const int item = item_of(r, blockIdx.x, gridDim.x, p.num_items, p.causal != 0);
-    if (item < 0) break;
-    const WorkItem w = decode_item(item, p);
+    Seg sg;
+    if (!seg_of<kSplit>(r, p, ctl->sk_range, sg)) break;
+    const WorkItem& w = sg.w;
     const int ntiles = w.n[q];
     if (ntiles == 0) continue;
     const int qtile = w.qt0 + q;
@@ -707,9 +889,13 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
     // when that P is published (the first P*V of an item overwrites O), and the read overlaps
     // this item's first Q*K^T, issued right after the previous item's last P*V.
     if (have_prev) {
-      uint32_t pk[64];
-      if (!epilogue_read(c, q, o_parity, 1.0f / l_prev, pk)) return;
-      epilogue_store(p, q, wp, row, m_prev, l_prev, pk);
+      if (kSplit && sp.slot >= 0) {
+        if (!epilogue_split(c, p, q, sp, row, m_prev, l_prev, o_parity)) return;
+      } else {
+        uint32_t pk[64];
+        if (!epilogue_read(c, q, o_parity, 1.0f / l_prev, pk)) return;
+        epilogue_store(p, q, sp.w, row, m_prev, l_prev, pk);
+      }
       o_parity ^= 1u;
     }
     float m_kept = 0.f;   // base-2 units; set on the first tile
@@ -724,10 +910,11 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
       // Masked columns (no weight): past the end of a key sequence that is not a multiple of
       // 128 (zero-filled key rows), and, with the causal mask, past this row on the diagonal
       // tile.  They must not enter the max and get P = 0 below.  The test is warp-uniform.
-      const bool diag = p.causal != 0 && j == qtile;
-      const bool partial = zero_scale || diag || (j == p.kv_tiles - 1 && p.kv_valid_last < kBlockN);
+      const int jg = sg.j0 + j;   // KV tile index within the head
+      const bool diag = p.causal != 0 && jg == qtile;
+      const bool partial = zero_scale || diag || (jg == p.kv_tiles - 1 && p.kv_valid_last < kBlockN);
       int valid = kBlockN;
-      if (j == p.kv_tiles - 1) valid = p.kv_valid_last;
+      if (jg == p.kv_tiles - 1) valid = p.kv_valid_last;
       if (diag) valid = min(valid, row + 1);
       if (partial) mask_scores(sr, valid, keep);
 
@@ -748,20 +935,25 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
       tphase ^= 1u;
     }
     have_prev = true;
-    wp = w;
+    sp = sg;
     m_prev = m_kept;
     l_prev = l;
   }
   if (have_prev) {
-    uint32_t pk[64];
-    if (!epilogue_read(c, q, o_parity, 1.0f / l_prev, pk)) return;
-    epilogue_store(p, q, wp, row, m_prev, l_prev, pk);
+    if (kSplit && sp.slot >= 0) {
+      epilogue_split(c, p, q, sp, row, m_prev, l_prev, o_parity);
+    } else {
+      uint32_t pk[64];
+      if (!epilogue_read(c, q, o_parity, 1.0f / l_prev, pk)) return;
+      epilogue_store(p, q, sp.w, row, m_prev, l_prev, pk);
+    }
   }
 }
 
 // ------------------------------------------------------------------ correction warpgroup
 // Per KV tile and stage: if any row of the warp rebased its max, O_q *= alpha in TMEM; then O_q
 // is safe for the next P*V (p_full, together with the softmax's P).
+template <bool kSplit>
 __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
   SmemCtl* ctl = c.ctl;
   const uint32_t row_base = 32u * (c.warp & 3u);
@@ -769,9 +961,9 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
   uint32_t tphase[2] = {0, 0};
 
   for (int r = 0;; ++r) {
-    const int item = item_of(r, blockIdx.x, gridDim.x, p.num_items, p.causal != 0);
-    if (item < 0) break;
-    const WorkItem w = decode_item(item, p);
+    Seg sg;
+    if (!seg_of<kSplit>(r, p, ctl->sk_range, sg)) break;
+    const WorkItem& w = sg.w;
     const int ntiles = w.n[1] > 0 ? w.n[1] : w.n[0];
     for (int j = 0; j < ntiles; ++j) {
 #pragma unroll
@@ -804,10 +996,10 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
 }
 
 // ------------------------------------------------------------------ kernel
-template <bool kSoftExp2>
+template <bool kSoftExp2, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const Params p) {
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -833,6 +1025,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     ptx::mbar_init(c.bar(ctl->drain), 1);
     ctl->abort_flag = 0;
+    if (kSplit) {
+      ctl->sk_range[0] = split_range_begin(blockIdx.x, gridDim.x, p.sk_items, p.kv_tiles);
+      ctl->sk_range[1] = split_range_begin(blockIdx.x + 1, gridDim.x, p.sk_items, p.kv_tiles);
+    }
     ptx::fence_mbar_init();
   }
   if (c.warp == kMmaWarp) {
@@ -853,14 +1049,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (threadIdx.x == 0) atomicOr(&g_attn_status, kStatusTmemBase);
   } else if (c.warp < kCorrWarp0) {
     ptx::setmaxnreg_inc<kRegSoftmax>();
-    softmax_role<kSoftExp2>(c, p, static_cast<int>(c.warp >> 2));
+    softmax_role<kSoftExp2, kSplit>(c, p, static_cast<int>(c.warp >> 2));
   } else if (c.warp < kLoadWarp) {
     ptx::setmaxnreg_dec<kRegCorr>();
-    correction_role(c, p);
+    correction_role<kSplit>(c, p);
   } else {
     ptx::setmaxnreg_dec<kRegMisc>();
-    if (c.warp == kLoadWarp) load_role(c, p, &tm_q, &tm_k, &tm_v);
-    else if (c.warp == kMmaWarp) mma_role(c, p);
+    if (c.warp == kLoadWarp) load_role<kSplit>(c, p, &tm_q, &tm_k, &tm_v);
+    else if (c.warp == kMmaWarp) mma_role<kSplit>(c, p);
   }
 
   ptx::tc_fence_before();

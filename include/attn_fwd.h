@@ -110,6 +110,59 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
                 int Sq, int Sk, int D, float scale, int flags, void* stream);
 
 /*
+ * attn_fwd_ws -- attn_fwd_ex with a workspace that lets the persistent grid end
+ * evenly.  Chapter 14 of "B200 Attention Kernel from Scratch to Near-SOTA in 60
+ * Diagrams" runs work items (a head and a pair of 128-row Q tiles) by static
+ * stride over one CTA per SM; when the item count is not a multiple of the grid,
+ * the last round leaves SMs idle (S=4K/8K/16K at 16 heads: 1024 items on 152
+ * SMs, 7 rounds for 6.74 rounds of work).  Here the items of the last two
+ * rounds are cut by KV range so that every CTA processes the same number of
+ * (item, 128-key tile) units; an item shared by two CTAs is finished from the
+ * two parts' partial results, O_i / l_i and log2-sum-exp L_i, as
+ * O = sum_i 2^(L_i - L) O_i / l_i with L = log2 sum_i 2^L_i -- the same
+ * rescaling of partial softmax sums that the online recurrence (Chapter 1,
+ * section B; Chapter 11) applies tile by tile.  Neither CTA waits for the
+ * other: the one that finishes second combines, always in KV order, so results
+ * are deterministic.  Output agrees with attn_fwd within rounding (the combined
+ * items round O once more in fp32).
+ *
+ *   q..stream        as attn_fwd_ex
+ *   workspace        device memory owned by the caller, 256-byte aligned, at
+ *                    least attn_fwd_workspace() bytes (0 bytes: NULL is fine);
+ *                    contents on entry are ignored and need no clearing
+ *   workspace_bytes  its size
+ *
+ * The split schedule is used for dense, non-causal calls without
+ * ATTN_FLAG_SOFT_EXP2 where it shortens the longest CTA by at least 12
+ * KV-tile iterations (each extra segment and the combine cost a few; on a
+ * 152-SM GPU: S=8K/16K at 16 heads and S=12K at 24 heads split, S=4K at 16
+ * heads does not); otherwise this is attn_fwd_ex and the workspace is not
+ * touched.  A
+ * workspace must not be used by two calls that can run at the same time
+ * (different streams): they would overwrite each other's partial results.
+ * Errors as attn_fwd_ex, plus ATTN_ERR_INVALID_ARG for a missing, short,
+ * misaligned or overlapping workspace when one is needed.
+ */
+int attn_fwd_ws(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int Sq, int Sk, int D, float scale, int flags, void* workspace,
+                size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace attn_fwd_ws needs for this problem on the current device
+ * (0 when it does not split; about 40 MB on a 152-SM GPU when it does). */
+int attn_fwd_workspace(int B, int H, int Sq, int Sk, int D, int flags, size_t* bytes);
+
+/* The schedule of attn_fwd_ws on the host, for tests: the segment a persistent
+ * CTA runs in its round-th turn for `work_items` items of `kv_tiles` KV tiles on
+ * `grid` CTAs.  Returns 1 and fills the outputs, 0 when the CTA has no more
+ * segments, ATTN_ERR_INVALID_ARG on bad arguments.  *kv_count == -1: the whole
+ * item (as attn_fwd_schedule); otherwise KV tiles [*kv_tile0, *kv_tile0 +
+ * *kv_count) of both Q tiles, and when that is not all of them, *slot >= 0 is
+ * the split's index and *part is 0 for the part holding KV tile 0, 1 for the
+ * other. */
+int attn_fwd_segment(int cta, int round, int grid, int64_t work_items, int kv_tiles, int flags,
+                     int* item, int* kv_tile0, int* kv_count, int* slot, int* part);
+
+/*
  * attn_fwd_host -- attn_fwd_ex with Q/K/V read from and O/LSE written to HOST
  * memory.  The pages' kernels take device tensors; this entry point is the
  * library's own end-to-end path for inputs that start on the host.

@@ -37,6 +37,16 @@ def _run(qb, kb, vb, scale, causal=False):
     return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
 
+def _fwd_whole_items(q, k, v, scale, causal=False, layout="bhsd"):
+    """attn_fwd_ex on device tensors (every work item whole in one CTA): the computation the
+    host-buffer entry point runs chunk by chunk."""
+    B, H, Sq, _, _ = attn._dims(q, k, layout)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, Sq, dtype=torch.float32, device=q.device)
+    attn.fwd_into(q, k, v, o, lse, scale, causal=causal, layout=layout)
+    return o, lse
+
+
 def _assert_close(o, o_ref, lse, lse_ref):
     err = np.abs(o - o_ref)
     lerr = np.abs(lse - lse_ref)
@@ -346,7 +356,7 @@ def test_host_buffer_forward_matches_device_path(shape, causal, layout, with_lse
         tens = [t.transpose(1, 2).contiguous() for t in tens]
     o_h, lse_h = attn.fwd(*tens, scale=0.1, causal=causal, layout=layout, return_lse=with_lse)
     assert not o_h.is_cuda and o_h.is_pinned()
-    o_d, lse_d = attn.fwd(*(t.cuda() for t in tens), scale=0.1, causal=causal, layout=layout)
+    o_d, lse_d = _fwd_whole_items(*(t.cuda() for t in tens), 0.1, causal=causal, layout=layout)
     torch.cuda.synchronize()
     assert torch.equal(o_h, o_d.cpu())
     if with_lse:
@@ -358,12 +368,12 @@ def test_host_buffer_forward_matches_device_path(shape, causal, layout, with_lse
 
 def test_host_buffer_forward_full_size():
     """S=4K (B=4, H=16) from host memory: chunks of 19/19/19/7 heads; bitwise equal to the
-    device path, sampled rows against the oracle."""
+    device path with whole items (attn_fwd_ex), sampled rows against the oracle."""
     w = wl.S4K
     qb, kb, vb = wl.workload_inputs_bits(w)
     tens = [wl.bits_to_torch(x).pin_memory() for x in (qb, kb, vb)]
     o_h, lse_h = attn.fwd(*tens, scale=w.scale)
-    o_d, lse_d = attn.fwd(*(t.cuda() for t in tens), scale=w.scale)
+    o_d, lse_d = _fwd_whole_items(*(t.cuda() for t in tens), w.scale)
     torch.cuda.synchronize()
     assert torch.equal(o_h, o_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
     bh, rows = _rows_sample(w, 100, seed=9)
@@ -375,7 +385,7 @@ def test_host_buffer_forward_full_size():
 
 def test_host_buffer_batch_matches_single_calls():
     """fwd_host_batch: several host-buffer problems in flight at once (own streams, shared copy
-    streams of the library); each result bitwise equal to its own device-path call."""
+    streams of the library); each result bitwise equal to its own device-path call (attn_fwd_ex)."""
     specs = [((2, 40, 1024, 1024), False, "bhsd"), ((3, 5, 300, 700), True, "bhsd"),
              ((9, 3, 640, 640), False, "bshd")]
     problems, expect = [], []
@@ -384,7 +394,7 @@ def test_host_buffer_batch_matches_single_calls():
         if layout == "bshd":
             tens = [t.transpose(1, 2).contiguous() for t in tens]
         problems.append(dict(q=tens[0], k=tens[1], v=tens[2], scale=0.09, causal=causal, layout=layout))
-        o_d, lse_d = attn.fwd(*(t.cuda() for t in tens), scale=0.09, causal=causal, layout=layout)
+        o_d, lse_d = _fwd_whole_items(*(t.cuda() for t in tens), 0.09, causal=causal, layout=layout)
         expect.append((o_d.cpu(), lse_d.cpu()))
     # the default order (most work per copied byte first) and two explicit ones
     for order in (None, [0, 1, 2], [2, 0, 1]):
@@ -392,3 +402,107 @@ def test_host_buffer_batch_matches_single_calls():
         for (o, lse), (o_e, lse_e) in zip(got, expect):
             assert torch.equal(o, o_e) and torch.equal(lse, lse_e)
     assert attn.device_status() == 0
+
+
+# ------------------------------------------------------------- split schedule (attn_fwd_ws)
+
+def _split_items(B, H, Sq, Sk, grid):
+    """Work items that attn_fwd_ws cuts by KV range (two parts in two CTAs)."""
+    p = attn.plan(B, H, Sq, Sk, 128, num_sms=grid)
+    n = p["kv_tiles"]
+    out = set()
+    for cta in range(p["grid"]):
+        r = 0
+        while (s := attn.segment(cta, r, p["grid"], p["work_items"], n)) is not None:
+            if s[3] >= 0:
+                out.add(s[0])
+            r += 1
+    return sorted(out)
+
+
+def _item_rows(B, H, Sq, Sk, items):
+    """(bh, row) of every query row of the given work items."""
+    bh, rows = [], []
+    for it in items:
+        b, qt0, n0, n1 = attn.work_item(it, B, H, Sq, Sk)
+        for t in (qt0, qt0 + 1) if n1 > 0 else (qt0,):
+            r = np.arange(t * 128, min((t + 1) * 128, Sq))
+            bh += [b] * len(r)
+            rows += list(r)
+    return np.array(bh, dtype=np.int64), np.array(rows, dtype=np.int64)
+
+
+@pytest.mark.parametrize("shape,layout", [
+    ((1, 40, 1024, 2048), "bhsd"),   # 160 items of 16 KV tiles on 152 SMs: all in the split part
+    ((2, 78, 512, 2048), "bhsd"),    # 312 items: one whole round, then the split part
+    ((1, 41, 1152, 2500), "bhsd"),   # odd Q-tile count (single-tile items), ragged last KV tile
+    ((1, 40, 1024, 2048), "bshd"),
+])
+def test_split_schedule_matches_oracle_and_whole_items(shape, layout):
+    """attn_fwd_ws against the oracle on every element; against attn_fwd_ex bitwise on the items
+    that run whole, within rounding on the split ones; bitwise the same from call to call."""
+    B, H, Sq, Sk = shape
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    split = _split_items(B, H, Sq, Sk, sms)
+    assert split, "the shape must exercise the split schedule"
+    qb, kb, vb = wl.make_inputs_bits(B, H, Sq, Sk, 128, seed=sum(shape))
+    scale = 1.0 / math.sqrt(128)
+    q, k, v = (wl.bits_to_torch(x).cuda() for x in (qb, kb, vb))
+    if layout == "bshd":
+        q, k, v = (t.transpose(1, 2).contiguous() for t in (q, k, v))
+    ws = attn.workspace_for(q, k, layout=layout)
+    assert ws is not None
+    outs = []
+    for workspace in (ws, ws, None):
+        o = torch.full_like(q, float("nan"))
+        lse = torch.full((B, H, Sq), float("nan"), device="cuda")
+        attn.fwd_into(q, k, v, o, lse, scale, layout=layout, workspace=workspace)
+        torch.cuda.synchronize()
+        if layout == "bshd":
+            o = o.transpose(1, 2)
+        outs.append((o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)))
+    (o1, l1), (o2, l2), (o0, l0) = outs
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    o_ref, lse_ref = oracle.attn_fwd(qb, kb, vb, scale)
+    _assert_close(o1, o_ref, l1, lse_ref)
+    bh, rows = _item_rows(B, H, Sq, Sk, split)
+    whole = np.ones((B * H, Sq), dtype=bool)
+    whole[bh, rows] = False
+    o1r, o0r = o1.reshape(B * H, Sq, 128), o0.reshape(B * H, Sq, 128)
+    l1r, l0r = l1.reshape(B * H, Sq), l0.reshape(B * H, Sq)
+    assert np.array_equal(o1r[whole], o0r[whole]) and np.array_equal(l1r[whole], l0r[whole])
+    # split items: the same softmax, summed in two parts (O rounded once more in fp32)
+    assert np.abs(o1r[~whole] - o0r[~whole]).max() <= 2 ** -7
+    assert np.abs(l1r[~whole] - l0r[~whole]).max() <= 1e-5 * max(1.0, np.abs(l0r).max())
+    assert attn.device_status() == 0
+
+
+def test_split_schedule_full_size_s8k_against_whole_items():
+    """The benchmark's S=8K launch (1024 items on the full grid) with and without the split."""
+    w = wl.ALL["S=8K"]
+    qb, kb, vb = wl.workload_inputs_bits(w)
+    q, k, v = (wl.bits_to_torch(x).cuda() for x in (qb, kb, vb))
+    ws = attn.workspace_for(q, k)
+    assert ws is not None
+    o1, l1 = torch.empty_like(q), torch.empty(w.B, w.H, w.Sq, device="cuda")
+    o0, l0 = torch.empty_like(q), torch.empty(w.B, w.H, w.Sq, device="cuda")
+    attn.fwd_into(q, k, v, o1, l1, w.scale, workspace=ws)
+    attn.fwd_into(q, k, v, o0, l0, w.scale)
+    torch.cuda.synchronize()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    split = _split_items(w.B, w.H, w.Sq, w.Sk, sms)
+    bh, rows = _item_rows(w.B, w.H, w.Sq, w.Sk, split)
+    mask = torch.ones(w.B * w.H, w.Sq, dtype=torch.bool)
+    mask[torch.as_tensor(bh), torch.as_tensor(rows)] = False
+    mask = mask.cuda()
+    o1r, o0r = o1.view(-1, w.Sq, 128), o0.view(-1, w.Sq, 128)
+    assert torch.equal(o1r[mask], o0r[mask]) and torch.equal(l1.view(-1, w.Sq)[mask], l0.view(-1, w.Sq)[mask])
+    d = (o1r[~mask].float() - o0r[~mask].float()).abs().max().item()
+    assert d <= 2 ** -7, d
+    # split rows against the oracle, a sample of them
+    rng = np.random.Generator(np.random.PCG64(11))
+    pick = rng.choice(len(bh), 300, replace=False)
+    o_ref, lse_ref = oracle.attn_fwd_rows(qb, kb, vb, w.scale, bh[pick], rows[pick])
+    o = o1r.float().cpu().numpy().astype(np.float64)[bh[pick], rows[pick]]
+    lse = l1.view(-1, w.Sq).cpu().numpy().astype(np.float64)[bh[pick], rows[pick]]
+    _assert_close(o, o_ref, lse, lse_ref)

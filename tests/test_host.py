@@ -202,6 +202,108 @@ def test_schedule_covers_every_item_once(lib):
     assert [attn.schedule(0, r, 148, 2048, causal=True) for r in range(3)] == [0, 295, 296]
 
 
+def _segments(cta, grid, items, n):
+    out, r = [], 0
+    while True:
+        s = attn.segment(cta, r, grid, items, n)
+        if s is None:
+            return out
+        out.append(s)
+        r += 1
+
+
+@pytest.mark.parametrize("items,grid,n", [
+    (1024, 152, 32), (1024, 152, 64), (1024, 152, 128),   # S=4K/8K/16K at 16 heads
+    (1152, 152, 96),                                     # S=12K, 24 heads: 7.58 rounds
+    (1216, 152, 8),                                      # whole rounds: no split
+    (400, 152, 3), (160, 152, 8), (301, 150, 5), (153, 152, 2), (1000, 7, 11),
+])
+def test_split_schedule_covers_every_unit_once_and_pairs_the_parts(lib, items, grid, n):
+    """attn_fwd_ws's schedule: every (item, KV tile) unit runs exactly once; an item cut by KV range
+    has exactly two parts, part 0 (from KV tile 0) ending the range of CTA `slot` and part 1
+    (through the last KV tile) starting the range of CTA `slot + 1`; no CTA runs more units than
+    the longest range of an even division of the last two rounds."""
+    units = {}
+    parts = {}
+    per_cta = []
+    for cta in range(grid):
+        segs = _segments(cta, grid, items, n)
+        total = 0
+        for k, (item, j0, cnt, slot, part) in enumerate(segs):
+            assert 0 <= item < items
+            if cnt == -1:
+                j0, cnt = 0, n
+            assert 0 <= j0 and j0 + cnt <= n and cnt >= 1
+            for j in range(j0, j0 + cnt):
+                assert (item, j) not in units, (item, j)
+                units[(item, j)] = cta
+            total += cnt
+            if cnt < n:
+                assert slot >= 0 and part == (1 if j0 > 0 else 0)
+                assert slot == (cta - 1 if part else cta) and 0 <= slot <= grid - 2
+                if part == 1:
+                    assert k == 0 or attn.segment(cta, k - 1, grid, items, n)[2] == -1  # first of the split rounds
+                else:
+                    assert k == len(segs) - 1 and j0 == 0
+                assert (slot, part) not in parts
+                parts[(slot, part)] = (item, j0, cnt)
+            else:
+                assert slot == -1
+        per_cta.append(total)
+    assert len(units) == items * n
+    for (slot, part), (item, j0, cnt) in parts.items():
+        other = parts[(slot, 1 - part)]
+        assert other[0] == item
+        lo, hi = (j0, j0 + cnt) if part == 0 else (other[1], other[1] + other[2])
+        assert lo == 0 and hi == (other[1] if part == 0 else j0)
+    full_rounds = -(-items // grid)
+    if items > grid and items % grid and parts:
+        sk0 = (items // grid - 1) * grid
+        longest = (sk0 // grid) * n + -(-(items - sk0) * n // grid)
+        assert max(per_cta) <= longest < full_rounds * n
+    else:
+        assert max(per_cta) == full_rounds * n
+
+
+def test_split_schedule_is_used_where_it_pays(lib):
+    # S=8K/16K at 16 heads and S=12K at 24 heads split (the longest CTA gets >= 12 KV tiles
+    # shorter); S=4K at 16 heads (8 tiles), whole rounds, short KV ranges and causal calls do not
+    def split(items, grid, n, causal=False):
+        for c in range(grid):
+            r = 0
+            while (s := attn.segment(c, r, grid, items, n, causal)) is not None:
+                if s[3] >= 0:
+                    return True
+                r += 1
+        return False
+
+    assert split(1024, 152, 64) and split(1024, 152, 128)
+    assert split(1152, 152, 96)   # S=12K at 24 heads: 7.58 rounds
+    assert not split(1024, 152, 32)
+    assert not split(1216, 152, 96) and not split(400, 152, 1) and not split(100, 152, 8)
+    assert not split(1024, 152, 64, causal=True)
+    # 1136 items: 7.47 rounds, but 64 KV tiles per item gain 34 tiles from an even division
+    assert split(1136, 152, 64)
+    # 1144 items: 7.53 rounds of 8 tiles gain under 12
+    assert not split(1144, 152, 8)
+
+
+def test_split_entry_point_checks_before_any_cuda_call(lib):
+    big = 1 << 40
+    vp = ctypes.c_void_p
+    args = (vp(big), vp(2 * big), vp(3 * big), vp(4 * big), None, 1, 1, 128, 128, 64, 0.1, 0)
+    assert lib.attn_fwd_ws(*args, None, 0, None) == attn.ATTN_ERR_UNSUPPORTED     # D = 64
+    args = (vp(big), vp(2 * big), vp(3 * big), vp(4 * big), None, 1, 1, 128, 128, 128, 0.1, 8)
+    assert lib.attn_fwd_ws(*args, None, 0, None) == attn.ATTN_ERR_INVALID_ARG     # bad flag
+    n = ctypes.c_size_t(7)
+    assert lib.attn_fwd_workspace(1, 1, 128, 128, 64, 0, ctypes.byref(n)) == attn.ATTN_ERR_UNSUPPORTED
+    assert lib.attn_fwd_workspace(0, 1, 128, 128, 128, 0, ctypes.byref(n)) == attn.ATTN_OK and n.value == 0
+    assert lib.attn_fwd_workspace(1, 1, 128, 128, 128, 0, None) == attn.ATTN_ERR_INVALID_ARG
+    out = [ctypes.c_int() for _ in range(5)]
+    assert lib.attn_fwd_segment(5, 0, 4, 10, 2, 0, *(ctypes.byref(x) for x in out)) == attn.ATTN_ERR_INVALID_ARG
+    assert lib.attn_fwd_segment(0, 0, 4, 10, 0, 0, *(ctypes.byref(x) for x in out)) == attn.ATTN_ERR_INVALID_ARG
+
+
 # ------------------------------------------------------------- host-buffer forward planning
 
 @pytest.mark.parametrize("B,H,S,expect", [
