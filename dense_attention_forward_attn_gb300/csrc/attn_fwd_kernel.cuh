@@ -766,8 +766,27 @@ __device__ __forceinline__ void epilogue_store(const Params& p, int q, const Wor
 // The combination is O = w0 O0/l0 + w1 O1/l1 with w_i = 2^(L_i - L), L = log2(2^L0 + 2^L1),
 // each product and the sum rounded separately, so it is the same whichever warp computes it.
 // Not inlined: it runs at most twice per CTA, and inlined into the softmax role it slowed the
-// whole-item rounds by 0.5-1% (larger loop code).
-__device__ __noinline__ bool epilogue_split(const Ctx& c, const Params& p, int q, const Seg& sg,
+// whole-item rounds by 0.5-1% (larger loop code).  It takes the few parameters it reads by value
+// (SplitOut): taking the address of the kernel's parameter block for a call made the compiler
+// read parameters through memory in the other roles as well.
+struct SplitOut {
+  float* ws_o;
+  float* ws_l;
+  unsigned long long* ws_flag;
+  unsigned long long seq;
+  void* o;
+  float* lse;
+  int64_t o_row_stride, o_head_stride, o_batch_stride;
+  int sq;
+  int heads;
+};
+
+__device__ __forceinline__ SplitOut split_out(const Params& p) {
+  return SplitOut{p.ws_o, p.ws_l, p.ws_flag, p.seq, p.o, p.lse, p.o_row_stride, p.o_head_stride,
+                  p.o_batch_stride, p.sq, p.heads};
+}
+
+__device__ __noinline__ bool epilogue_split(const Ctx& c, const SplitOut p, int q, const Seg& sg,
                                                int row, float m, float l, uint32_t o_parity) {
   if (!c.wait(c.ctl->o_full[q], o_parity, kStatusTimeoutSoftmax)) return false;
   ptx::tc_fence_after();
@@ -890,7 +909,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
     // this item's first Q*K^T, issued right after the previous item's last P*V.
     if (have_prev) {
       if (kSplit && sp.slot >= 0) {
-        if (!epilogue_split(c, p, q, sp, row, m_prev, l_prev, o_parity)) return;
+        if (!epilogue_split(c, split_out(p), q, sp, row, m_prev, l_prev, o_parity)) return;
       } else {
         uint32_t pk[64];
         if (!epilogue_read(c, q, o_parity, 1.0f / l_prev, pk)) return;
@@ -941,7 +960,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
   }
   if (have_prev) {
     if (kSplit && sp.slot >= 0) {
-      epilogue_split(c, p, q, sp, row, m_prev, l_prev, o_parity);
+      epilogue_split(c, split_out(p), q, sp, row, m_prev, l_prev, o_parity);
     } else {
       uint32_t pk[64];
       if (!epilogue_read(c, q, o_parity, 1.0f / l_prev, pk)) return;
@@ -999,7 +1018,7 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
 template <bool kSoftExp2, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ Params p) {
+                const __grid_constant__ CUtensorMap tm_v, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
