@@ -763,6 +763,7 @@ __device__ __forceinline__ void epilogue_store(const Params& p, int q, const Wor
 // combines at once.  Otherwise it writes its own part there and swaps the sequence number into
 // the flag; if that swap returns the number, the partner wrote in the meantime and this warp
 // combines, else the partner will.  Exactly one of the two warps combines, and neither waits.
+// The combining warp clears the flag again.
 // The combination is O = w0 O0/l0 + w1 O1/l1 with w_i = 2^(L_i - L), L = log2(2^L0 + 2^L1),
 // each product and the sum rounded separately, so it is the same whichever warp computes it.
 // Not inlined: it runs at most twice per CTA, and inlined into the softmax role it slowed the
@@ -829,6 +830,9 @@ __device__ __noinline__ bool epilogue_split(const Ctx& c, const SplitOut p, int 
     }
   }
   __threadfence();
+  // Both parts have arrived and nothing else touches this flag in this launch: clear it, so a later
+  // launch with the same sequence number (a replayed CUDA graph) does not take it for its partner.
+  if (c.lane == 0) *flag = 0ull;
   // Combine: this part from TMEM (O / l recomputed exactly as stored), the other from the workspace.
   const float L_oth = __ldcg(p.ws_l + oth * kBlockM + row);
   const float L0 = sg.part == 0 ? L_own : L_oth, L1 = sg.part == 0 ? L_oth : L_own;

@@ -129,7 +129,12 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
  *   q..stream        as attn_fwd_ex
  *   workspace        device memory owned by the caller, 256-byte aligned, at
  *                    least attn_fwd_workspace() bytes (0 bytes: NULL is fine);
- *                    contents on entry are ignored and need no clearing
+ *                    contents on entry are ignored and need no clearing.  Each
+ *                    call tags its flags there with a number unique to the call
+ *                    and clears every flag it completed, so a launch that reuses
+ *                    the number (a replayed CUDA graph) finds them clear; after a
+ *                    call that reported an expired wait (attn_device_status),
+ *                    zero the workspace before replaying such a launch on it
  *   workspace_bytes  its size
  *
  * The split schedule is used for dense, non-causal calls without

@@ -582,3 +582,37 @@ def test_split_schedule_workspace_is_checked():
     os_, _ = _split_call(qs, qs, qs, 0.1, workspace=None)
     torch.cuda.synchronize()
     assert torch.isfinite(os_.float()).all()
+
+
+def test_split_schedule_replayed_in_a_cuda_graph():
+    """attn_fwd_ws captured once in a CUDA graph (one sequence number for every replay) and
+    replayed on new input data: each replay equals the whole-item path on that data, so no replay
+    combines its parts with an earlier replay's partial results."""
+    B, H, Sq, Sk = 1, 40, 1024, 2048
+    q = torch.randn(B, H, Sq, 128, device="cuda").bfloat16()
+    k = torch.randn(B, H, Sk, 128, device="cuda").bfloat16()
+    v = torch.randn(B, H, Sk, 128, device="cuda").bfloat16()
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, Sq, device="cuda")
+    ws = attn.workspace_for(q, k)
+    assert ws is not None
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        attn.fwd_into(q, k, v, o, lse, 0.1, workspace=ws)   # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        attn.fwd_into(q, k, v, o, lse, 0.1, workspace=ws)
+    for rep in range(3):
+        gen = torch.Generator(device="cuda").manual_seed(100 + rep)
+        for t in (q, k, v):
+            t.copy_(torch.randn(t.shape, device="cuda", generator=gen).bfloat16())
+        g.replay()
+        o_ref, lse_ref = _fwd_whole_items(q, k, v, 0.1)
+        torch.cuda.synchronize()
+        d = (o.float() - o_ref.float()).abs().max().item()
+        assert d <= 2 ** -7, (rep, d)
+        assert (lse - lse_ref).abs().max().item() <= 1e-4
+    assert attn.device_status() == 0
