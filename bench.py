@@ -151,12 +151,18 @@ def _dist():
 
 
 def _source_sha() -> str:
-    """Hash of the forward kernel's device source (the files its code is compiled from)."""
+    """Hash of the forward kernel's device source (the files its code is compiled from), with
+    comments and blank lines removed, so that only code changes make a recorded profile stale."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_attention_forward_attn_gb300", "csrc")
     for name in ("attn_fwd_kernel.cuh", "ptx.cuh"):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(name.encode() + code.encode())
     return h.hexdigest()[:16]
 
 
