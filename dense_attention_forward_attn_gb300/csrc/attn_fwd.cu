@@ -609,6 +609,20 @@ int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* l
 
 }  // extern "C"
 
+// The backward's two gradient kernels are independent once delta is written; the dQ kernel runs
+// on a side stream of the library so its CTAs can take the SMs that the dK/dV kernel's last,
+// partly filled wave leaves idle (and the other way round), instead of each kernel ending on its
+// own partial wave.  One side stream and a fork/join event pair per device, created on first use.
+namespace {
+struct BwdFork {
+  bool ready = false;
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+BwdFork g_bwd_fork[kMaxDevices];
+std::mutex g_bwd_mu;
+}  // namespace
+
 extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void* o,
                         const void* dout, const float* lse, void* dq, void* dk, void* dv,
                         float* delta, int B, int H, int Sq, int Sk, int D, float scale, int flags,
@@ -693,6 +707,23 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   attn::bwd::attn_bwd_delta_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
       static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), delta, rows, H, Sq,
       p.bshd);
+  std::lock_guard<std::mutex> lk(g_bwd_mu);
+  BwdFork& F = g_bwd_fork[dev];
+  if (!F.ready) {
+    if (cudaStreamCreateWithFlags(&F.side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&F.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&F.join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    F.ready = true;
+  }
+  // dQ waits for delta (and for everything queued on the caller's stream before it); the
+  // caller's stream waits for dQ before anything it runs next.
+  if (cudaEventRecord(F.fork, st) != cudaSuccess || cudaStreamWaitEvent(F.side, F.fork, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
   p.out0 = dk;
   p.out1 = dv;
   attn::bwd::attn_bwd_dkdv_kernel<<<static_cast<unsigned>(bh * p.kv_tiles), attn::bwd::kThreads,
@@ -701,10 +732,15 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   p.out0 = dq;
   p.out1 = nullptr;
   attn::bwd::attn_bwd_dq_kernel<<<static_cast<unsigned>(bh * ((p.q_tiles + 1) / 2)),
-                                  attn::bwd::kDqThreads, attn::bwd::kSmemBytesDq, st>>>(
+                                  attn::bwd::kDqThreads, attn::bwd::kSmemBytesDq, F.side>>>(
       tm_q, tm_k, tm_v, tm_do, p);
-  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-  return ATTN_OK;
+  const bool launched = cudaGetLastError() == cudaSuccess;
+  // Join even after a failed launch, so the caller's stream never runs ahead of a dQ in flight.
+  if (cudaEventRecord(F.join, F.side) != cudaSuccess || cudaStreamWaitEvent(st, F.join, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  return launched ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ allocation-free backward

@@ -237,7 +237,11 @@ int attn_fwd_host_chunking(int B, int H, int Sq, int Sk, int flags, int num_sms,
  * ownership and error rules as attn_fwd; no output may overlap any input or
  * another output.  Sq == 0 zero-fills dk and dv.  Deterministic: every
  * gradient element is written by exactly one thread, no atomics.
- * Asynchronous: three kernels (delta, dk/dv, dq) are enqueued in order.
+ * Asynchronous: three kernels.  delta, then dk/dv, on `stream`; dq on an
+ * internal stream of the library (one per device) that first waits for the
+ * work on `stream` up to delta, so the two gradient kernels share the GPU;
+ * `stream` then waits for dq.  Everything the call enqueues completes before
+ * any later work on `stream` starts, as if all three ran on it.
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
              const float* lse, void* dq, void* dk, void* dv, float* delta, int B, int H,
