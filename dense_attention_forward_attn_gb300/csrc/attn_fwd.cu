@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstring>
 #include <atomic>
+#include <chrono>
 #include <mutex>
 #include <random>
 
@@ -194,8 +195,16 @@ SplitPlan split_plan(int64_t items, int grid, int kv_tiles, int flags) {
 unsigned long long next_seq() {
   static std::atomic<unsigned long long> counter{0};
   static const unsigned long long salt = [] {
-    std::random_device rd;
-    return (static_cast<unsigned long long>(rd()) | 1ull) << 32;
+    unsigned long long r;
+    try {
+      std::random_device rd;
+      r = rd();
+    } catch (...) {   // no entropy source: the clock and this object's address instead
+      r = static_cast<unsigned long long>(
+              std::chrono::high_resolution_clock::now().time_since_epoch().count()) ^
+          reinterpret_cast<uintptr_t>(&counter);
+    }
+    return ((r & 0xffffffffull) | 1ull) << 32;
   }();
   return salt + counter.fetch_add(1, std::memory_order_relaxed);
 }

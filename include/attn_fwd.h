@@ -241,7 +241,9 @@ int attn_fwd_host_chunking(int B, int H, int Sq, int Sk, int flags, int num_sms,
  * internal stream of the library (one per device) that first waits for the
  * work on `stream` up to delta, so the two gradient kernels share the GPU;
  * `stream` then waits for dq.  Everything the call enqueues completes before
- * any later work on `stream` starts, as if all three ran on it.
+ * any later work on `stream` starts, as if all three ran on it.  The internal
+ * stream is shared by every call on the device, so dq kernels of calls made
+ * on different streams run one after another.
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
              const float* lse, void* dq, void* dk, void* dv, float* delta, int B, int H,
