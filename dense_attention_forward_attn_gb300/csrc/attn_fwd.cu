@@ -59,9 +59,13 @@ int device_info(int dev, DeviceInfo* out) {
     return fa.numRegs == want;
   };
   if (!d.attr_set) {
-    const void* fwd_kernels[] = {reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false>),
-                                 reinterpret_cast<const void*>(attn::attn_fwd_kernel<true, false>),
-                                 reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true>)};
+    const void* fwd_kernels[] = {
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<true, false, false>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, false>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, true>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<true, false, true>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, true>)};
     for (const void* fn : fwd_kernels) {
       if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(attn::kSmemBytes)) != cudaSuccess) {
@@ -438,16 +442,22 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
     p.seq = next_seq();
   }
 
+  // Instantiations: <software exp2, split schedule, [B,S,H,D]>; the split schedule is never
+  // used with the software exp2.
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (sp.on)
-    attn::attn_fwd_kernel<false, true><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tm_q, tm_k,
-                                                                                      tm_v, p);
-  else if (flags & ATTN_FLAG_SOFT_EXP2)
-    attn::attn_fwd_kernel<true, false><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tm_q, tm_k,
-                                                                                      tm_v, p);
-  else
-    attn::attn_fwd_kernel<false, false><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tm_q, tm_k,
-                                                                                       tm_v, p);
+  const bool soft = (flags & ATTN_FLAG_SOFT_EXP2) != 0;
+#define ATTN_LAUNCH(S, P, L) \
+  attn::attn_fwd_kernel<S, P, L><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tm_q, tm_k, tm_v, p)
+  if (bshd) {
+    if (sp.on) ATTN_LAUNCH(false, true, true);
+    else if (soft) ATTN_LAUNCH(true, false, true);
+    else ATTN_LAUNCH(false, false, true);
+  } else {
+    if (sp.on) ATTN_LAUNCH(false, true, false);
+    else if (soft) ATTN_LAUNCH(true, false, false);
+    else ATTN_LAUNCH(false, false, false);
+  }
+#undef ATTN_LAUNCH
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
