@@ -358,3 +358,30 @@ def test_host_batch_order_puts_most_work_per_byte_first():
     assert attn.batch_order(probs) == [0, 1, 2]
     with pytest.raises(ValueError):
         attn.fwd_host_batch(probs, order=[0, 0, 1])
+
+
+def test_bench_source_hash_ignores_comments(tmp_path, monkeypatch):
+    """The hash that decides whether the recorded DRAM traffic still describes the kernel changes
+    with the kernel's code, not with its comments or blank lines."""
+    import shutil
+    import bench
+    csrc = tmp_path / "dense_attention_forward_attn_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    src = os.path.join(ROOT, "dense_attention_forward_attn_gb300", "csrc")
+    for name in ("attn_fwd_kernel.cuh", "ptx.cuh"):
+        shutil.copy(os.path.join(src, name), csrc / name)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    base = bench._source_sha()
+    k = csrc / "attn_fwd_kernel.cuh"
+    text = k.read_text()
+    k.write_text("// a new comment\n\n" + text.replace("namespace attn {", "namespace attn {  /* note */", 1))
+    assert bench._source_sha() == base
+    k.write_text(text.replace("kRebaseThresholdLog2 = 8.0f", "kRebaseThresholdLog2 = 7.0f", 1))
+    assert bench._source_sha() != base
+
+
+def test_workspace_query_needs_no_launch(lib):
+    # empty problems need no workspace; a bad head size is refused before any CUDA call
+    assert attn.workspace_bytes(0, 16, 4096, 4096) == 0
+    with pytest.raises(attn.AttnError):
+        attn.workspace_bytes(1, 1, 128, 128, D=64)
