@@ -433,10 +433,10 @@ def _item_rows(B, H, Sq, Sk, items):
 
 
 @pytest.mark.parametrize("shape,layout", [
-    ((1, 40, 1024, 2048), "bhsd"),   # 160 items of 16 KV tiles on 152 SMs: all in the split part
-    ((2, 78, 512, 2048), "bhsd"),    # 312 items: one whole round, then the split part
-    ((1, 41, 1152, 2500), "bhsd"),   # odd Q-tile count (single-tile items), ragged last KV tile
-    ((1, 40, 1024, 2048), "bshd"),
+    ((1, 40, 1024, 4096), "bhsd"),   # 160 items of 32 KV tiles on 152 SMs: all in the split part
+    ((2, 78, 512, 4096), "bhsd"),    # 312 items: one whole round, then the split part
+    ((1, 41, 1152, 6000), "bhsd"),   # odd Q-tile count (single-tile items), ragged last KV tile
+    ((1, 40, 1024, 4096), "bshd"),
 ])
 def test_split_schedule_matches_oracle_and_whole_items(shape, layout):
     """attn_fwd_ws against the oracle on every element; against attn_fwd_ex bitwise on the items
@@ -477,9 +477,9 @@ def test_split_schedule_matches_oracle_and_whole_items(shape, layout):
     assert attn.device_status() == 0
 
 
-def test_split_schedule_full_size_s8k_against_whole_items():
-    """The benchmark's S=8K launch (1024 items on the full grid) with and without the split."""
-    w = wl.ALL["S=8K"]
+def test_split_schedule_full_size_s16k_against_whole_items():
+    """The benchmark's S=16K launch (1024 items on the full grid) with and without the split."""
+    w = wl.ALL["S=16K"]
     qb, kb, vb = wl.workload_inputs_bits(w)
     q, k, v = (wl.bits_to_torch(x).cuda() for x in (qb, kb, vb))
     ws = attn.workspace_for(q, k)
@@ -520,11 +520,12 @@ def _split_call(q, k, v, scale, lse=True, workspace="auto"):
 def test_split_schedule_stress_logits_ragged_queries_and_no_lse():
     """Split items whose two parts keep very different row maxima (stress logits: Q, K ~ N(0, 3^2)
     with every 64th key x8), a ragged last Q tile (rows past Sq are not outputs), and the call
-    without an LSE buffer, which must give the same O bitwise.  V ~ N(0, 0.5^2): with 2,500 keys
+    without an LSE buffer, which must give the same O bitwise.  V ~ N(0, 0.5^2): with 6,000 keys
     and these logits most rows copy one V row, and with V ~ N(0, 1) the pages' rounding alone (BF16
-    P over an fp32 row sum, BF16 O) reaches 0.024 max-abs on this input for whole items as well (a
-    CPU emulation of that rounding gives 0.0237 for both schedules, and 0.0119 at this V scale)."""
-    B, H, Sq, Sk = 1, 41, 1100, 2500
+    P over an fp32 row sum, BF16 O) reaches 0.025 max-abs on this input for whole items as well (a
+    CPU emulation of that rounding gives 0.0250 whole and 0.0205 split, and 0.0125 / 0.0102 at
+    this V scale)."""
+    B, H, Sq, Sk = 1, 41, 1100, 6000
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert _split_items(B, H, Sq, Sk, sms)
     qb, kb, vb = wl.make_inputs_bits(B, H, Sq, Sk, 128, seed=77, qk_std=3.0, spike_every=64,
@@ -542,7 +543,7 @@ def test_split_schedule_stress_logits_ragged_queries_and_no_lse():
 
 
 def test_split_schedule_zero_scale_is_uniform_average():
-    B, H, Sq, Sk = 1, 40, 1024, 2048
+    B, H, Sq, Sk = 1, 40, 1024, 4096
     qb, kb, vb = wl.make_inputs_bits(B, H, Sq, Sk, 128, seed=78)
     q, k, v = (wl.bits_to_torch(x).cuda() for x in (qb, kb, vb))
     o, lse = _split_call(q, k, v, 0.0)
@@ -556,7 +557,7 @@ def test_split_schedule_zero_scale_is_uniform_average():
 def test_split_schedule_workspace_is_checked():
     """A short, misaligned or overlapping workspace is refused before anything is launched; where
     the schedule does not split, none is needed."""
-    B, H, Sq, Sk = 1, 40, 1024, 2048
+    B, H, Sq, Sk = 1, 40, 1024, 4096
     q = torch.randn(B, H, Sq, 128, device="cuda").bfloat16()
     k = torch.randn(B, H, Sk, 128, device="cuda").bfloat16()
     n = attn.workspace_bytes(B, H, Sq, Sk)
@@ -588,7 +589,7 @@ def test_split_schedule_replayed_in_a_cuda_graph():
     """attn_fwd_ws captured once in a CUDA graph (one sequence number for every replay) and
     replayed on new input data: each replay equals the whole-item path on that data, so no replay
     combines its parts with an earlier replay's partial results."""
-    B, H, Sq, Sk = 1, 40, 1024, 2048
+    B, H, Sq, Sk = 1, 40, 1024, 4096
     q = torch.randn(B, H, Sq, 128, device="cuda").bfloat16()
     k = torch.randn(B, H, Sk, 128, device="cuda").bfloat16()
     v = torch.randn(B, H, Sk, 128, device="cuda").bfloat16()
