@@ -437,6 +437,7 @@ def _item_rows(B, H, Sq, Sk, items):
     ((2, 78, 512, 4096), "bhsd"),    # 312 items: one whole round, then the split part
     ((1, 41, 1152, 6000), "bhsd"),   # odd Q-tile count (single-tile items), ragged last KV tile
     ((1, 40, 1024, 4096), "bshd"),
+    ((1, 40, 1024, 4000), "bshd"),   # [B,S,H,D] with a ragged last KV tile (32 keys) in each second part
 ])
 def test_split_schedule_matches_oracle_and_whole_items(shape, layout):
     """attn_fwd_ws against the oracle on every element; against attn_fwd_ex bitwise on the items
