@@ -213,6 +213,26 @@ def test_online_recurrence_reaches_plain_definition(block_n):
     assert (reb >= 1).all()
 
 
+@pytest.mark.parametrize("split", [128, 384, 640])
+def test_kv_split_combine_reproduces_the_whole_softmax(split):
+    """The reading the split schedule follows: an item's KV range cut into [0, x) and [x, n), each
+    part run through the pages' online recurrence on its own (its own kept max and row sum), then
+    combined with L_i = m_i + log2 l_i, L = log2(2^L0 + 2^L1), O = sum_i 2^(L_i - L) O_i / l_i,
+    equals the softmax over all keys, and L ln 2 is its LSE."""
+    qb, kb, vb = wl.make_inputs_bits(1, 1, 96, 768, 128, seed=12, qk_std=2.0)
+    scale = 1.0 / math.sqrt(128)
+    q, k, v = (online.bf16_bits_to_f64(x)[0, 0] for x in (qb, kb, vb))
+    parts = []
+    for lo, hi in ((0, split), (split, 768)):
+        o_i, _, _, m_i, l_i = online.online_attention_head(q, k[lo:hi], v[lo:hi], scale)
+        parts.append((o_i, m_i + np.log2(l_i)))
+    L = np.logaddexp2(parts[0][1], parts[1][1])
+    o = sum(np.exp2(L_i - L)[:, None] * o_i for o_i, L_i in parts)
+    o_ref, lse_ref = oracle.attn_fwd(qb, kb, vb, scale)
+    assert np.abs(o - o_ref[0, 0]).max() <= 1e-12
+    assert np.abs(L * math.log(2.0) - lse_ref[0, 0]).max() <= 1e-12
+
+
 def test_online_recurrence_threshold_never_and_always():
     qb, kb, vb = wl.make_inputs_bits(1, 1, 16, 512, 64, seed=13, qk_std=2.0)
     scale = 0.125
