@@ -324,9 +324,11 @@ def test_bshd_layout(shape, causal):
     assert torch.equal(o2, o.transpose(1, 2).contiguous()) and torch.equal(lse2, lse)
 
 
-def test_bshd_full_size_sampled_rows():
-    """S=4K (B=4, H=16) in [B,S,H,D]: sampled rows against the oracle, bitwise equal to BHSD."""
-    w = wl.S4K
+@pytest.mark.parametrize("name", ["S=4K", "S=16K"])
+def test_bshd_full_size_sampled_rows(name):
+    """The benchmark's [B,S,H,D] launches (S=4K whole items, S=16K the split schedule): sampled rows
+    against the oracle, bitwise equal to [B,H,S,D]."""
+    w = wl.ALL[name]
     qb, kb, vb = wl.workload_inputs_bits(w)
     q, k, v = (wl.bits_to_torch(np.ascontiguousarray(x.transpose(0, 2, 1, 3))).cuda() for x in (qb, kb, vb))
     o, lse = attn.fwd(q, k, v, scale=w.scale, layout="bshd")
