@@ -790,6 +790,11 @@ extern "C" int attn_bwd_noalloc(const void* q, const void* k, const void* v, con
     cudaGetLastError();
     return ATTN_ERR_CUDA;
   }
+  // The device checks first (architecture, kernel attributes), so a device this library does not
+  // run on reports ATTN_ERR_ARCH as attn_bwd does, before the array's address is looked up.
+  DeviceInfo info;
+  const int rc = device_info(dev, &info);
+  if (rc != ATTN_OK) return rc;
   float* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lk(g_noalloc_mu);

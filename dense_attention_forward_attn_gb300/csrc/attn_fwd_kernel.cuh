@@ -721,7 +721,8 @@ __device__ __forceinline__ float row_max_128(const uint32_t (&sr)[4][32]) {
 }
 
 // Item epilogue of stage q, run by the stage's own softmax warpgroup: O_q (final once the item's
-// last P*V is done, o_full) is read from TMEM, scaled by 1/l and packed to BF16 in registers;
+// last P*V is done, o_full) is read from TMEM, scaled by 1 / (row sum of the BF16 weights) and
+// packed to BF16 in registers;
 // once read, O_q's columns are free for the next item's first P*V, which waits for the next
 // P this warpgroup publishes.  The stores to global memory follow from the registers.
 __device__ __forceinline__ bool epilogue_read(const Ctx& c, int q, uint32_t o_parity, float inv_l,
@@ -744,7 +745,7 @@ __device__ __forceinline__ bool epilogue_read(const Ctx& c, int q, uint32_t o_pa
 }
 
 // O row and LSE of this thread's query row of stage q of item w (rows past a ragged end of Q
-// are computed but not stored).  LSE = (kept max + log2 l) * ln 2.
+// are computed but not stored).  LSE = (kept max + log2 l) * ln 2, l the row sum of the fp32 P.
 __device__ __forceinline__ void epilogue_store(const Params& p, int q, const WorkItem& w, int row,
                                                float m, float l, const uint32_t (&pk)[64]) {
   const int grow = (w.qt0 + q) * kBlockM + row;
@@ -790,18 +791,20 @@ __device__ __forceinline__ SplitOut split_out(const Params& p) {
 }
 
 __device__ __noinline__ bool epilogue_split(const Ctx& c, const SplitOut p, int q, const Seg& sg,
-                                               int row, float m, float l, uint32_t o_parity) {
+                                               int row, float m, float l, float l_bf16,
+                                               uint32_t o_parity) {
   if (!c.wait(c.ctl->o_full[q], o_parity, kStatusTimeoutSoftmax)) return false;
   ptx::tc_fence_after();
   const uint32_t taddr_o = c.tmem + ((32u * (c.warp & 3u)) << 16) + col_o(q);
-  const float inv_l = 1.0f / l;
-  const float L_own = m + log2f(l);
+  const float inv_l = 1.0f / l_bf16;   // O / l with the row sum of the weights P*V used
+  const float L_own = m + log2f(l);     // the part's log2-sum-exp, from the fp32 row sum
   constexpr size_t kPartFloats = static_cast<size_t>(kBlockM) * kHeadDim;
   const size_t own = (static_cast<size_t>(sg.slot) * 2 + sg.part) * 2 + q;   // [slot][part][stage]
   const size_t oth = (static_cast<size_t>(sg.slot) * 2 + (1 - sg.part)) * 2 + q;
   unsigned long long* flag = p.ws_flag + (static_cast<size_t>(sg.slot) * 2 + q) * 4 + (c.warp & 3u);
   unsigned long long f = 0;
   if (c.lane == 0) f = ptx::ld_acquire_u64(flag);
+  __syncwarp();   // orders lane 0's acquire before the other lanes' reads of the partner's part
   f = __shfl_sync(0xffffffffu, f, 0);
   if (f != p.seq) {
     float* dst = p.ws_o + own * kPartFloats + row * 4;   // chunk i (4 columns) at + i * 128 * 4
@@ -825,6 +828,7 @@ __device__ __noinline__ bool epilogue_split(const Ctx& c, const SplitOut p, int 
       f = atomicExch(flag, p.seq);
       __threadfence();
     }
+    __syncwarp();
     f = __shfl_sync(0xffffffffu, f, 0);
     if (f != p.seq) {   // the partner combines
       ptx::tc_fence_before();
@@ -901,7 +905,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
   uint32_t o_parity = 0;     // o_full phase of the previous item
   bool have_prev = false;    // an item whose epilogue is still to do
   Seg sp;
-  float m_prev = 0.f, l_prev = 1.f;
+  float m_prev = 0.f, l_prev = 1.f, lr_prev = 1.f;
 
   for (int r = 0;; ++r) {
     Seg sg;
@@ -915,16 +919,17 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
     // this item's first Q*K^T, issued right after the previous item's last P*V.
     if (have_prev) {
       if (kSplit && sp.slot >= 0) {
-        if (!epilogue_split(c, split_out(p), q, sp, row, m_prev, l_prev, o_parity)) return;
+        if (!epilogue_split(c, split_out(p), q, sp, row, m_prev, l_prev, lr_prev, o_parity)) return;
       } else {
         uint32_t pk[64];
-        if (!epilogue_read(c, q, o_parity, 1.0f / l_prev, pk)) return;
+        if (!epilogue_read(c, q, o_parity, 1.0f / lr_prev, pk)) return;
         epilogue_store(p, q, sp.w, row, m_prev, l_prev, pk);
       }
       o_parity ^= 1u;
     }
     float m_kept = 0.f;   // base-2 units; set on the first tile
-    float l = 0.f;
+    float l = 0.f;    // row sum of the fp32 P (for the LSE)
+    float dl = 0.f;   // BF16 rounding of the largest P of each tile (see below)
     for (int j = 0; j < ntiles; ++j) {
       if (!c.wait(ctl->s_full[q], tphase, kStatusTimeoutSoftmax)) return;
       ptx::tc_fence_after();
@@ -944,32 +949,41 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
       if (partial) mask_scores(sr, valid, keep);
 
       // Row max over the raw scores: a 3-input-max tree (depth 5, 65 instructions).
-      const float m_tile = row_max_128(sr) * scale_log2;
+      const float s_max = row_max_128(sr);
+      const float m_tile = s_max * scale_log2;
       float alpha = 1.f;
       if (j == 0) {
         m_kept = m_tile;
       } else if (m_tile - m_kept >= kRebaseThresholdLog2) {
         alpha = ptx::ex2_ftz(m_kept - m_tile);
         l *= alpha;
+        dl *= alpha;
         m_kept = m_tile;
       }
       ctl->alpha[q][tphase][row] = alpha;
       c.arrive(ctl->stats_full[q]);
 
       l += produce_p<kSoftExp2>(c, q, sr, scale_log2, m_kept, taddr_s);
+      // P*V multiplies the BF16-rounded P, the row sum l adds the fp32 P.  O is divided by
+      // l + dl, where dl carries the rounding (BF16 minus fp32) of the tile's largest P, the same
+      // value produce_p computed for that column: numerator and denominator then agree on the
+      // weight that dominates a peaked row, while the LSE keeps the exact fp32 sum.
+      const float p_top = ptx::ex2_ftz(fmaf(s_max, scale_log2, -m_kept));
+      dl += __uint_as_float(ptx::pack_bf16x2(0.f, p_top)) - p_top;
       tphase ^= 1u;
     }
     have_prev = true;
     sp = sg;
     m_prev = m_kept;
     l_prev = l;
+    lr_prev = l + dl;
   }
   if (have_prev) {
     if (kSplit && sp.slot >= 0) {
-      epilogue_split(c, split_out(p), q, sp, row, m_prev, l_prev, o_parity);
+      epilogue_split(c, split_out(p), q, sp, row, m_prev, l_prev, lr_prev, o_parity);
     } else {
       uint32_t pk[64];
-      if (!epilogue_read(c, q, o_parity, 1.0f / l_prev, pk)) return;
+      if (!epilogue_read(c, q, o_parity, 1.0f / lr_prev, pk)) return;
       epilogue_store(p, q, sp.w, row, m_prev, l_prev, pk);
     }
   }

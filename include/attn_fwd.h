@@ -258,16 +258,22 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
  * synchronise the device.  attn_bwd needs a [B, H, Sq] fp32 scratch buffer
  * (delta); this entry point takes no such buffer and uses a fixed array
  * compiled into the library instead, so it allocates nothing: no cudaMalloc,
- * cudaFree or allocating library call, on any call.
+ * cudaFree or allocating library call, on any call (see below for what the
+ * first call on a device sets up).
  *
  * Arguments as attn_bwd without `delta`.  Limit: B * H * Sq <= 1,048,576
  * (the array is 4 MiB); larger problems return ATTN_ERR_TOO_LARGE without
  * launching.  Every GPU that loads the library holds the 4 MiB array until the
  * process exits.
  *
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.  All calls share the one array: two calls whose kernels
+ * The first call on a device does the library's one-time set-up for that
+ * device, with that device current: it checks the device and sets the kernels'
+ * attributes (as the first call of any entry point here does), looks up the
+ * array's device address (cudaGetSymbolAddress, which may load the library's
+ * device code and place the array), and creates the internal stream and two
+ * events the backward uses (as attn_bwd's first call does).  None of these
+ * allocate through cudaMalloc, but they are not capturable: make that first call
+ * before any stream capture.  All calls share the one array: two calls whose kernels
  * overlap on the GPU (different streams, no ordering between them) race on it
  * and give wrong gradients.  Calls ordered on one stream are safe; the array
  * keeps the last call's contents, which the next call overwrites before reading.

@@ -79,10 +79,11 @@ def test_backward_deterministic():
     assert all(torch.equal(x, y) for x, y in zip(a, b))
 
 
-@pytest.mark.parametrize("name", ["S=4K", "S=8K"])   # one S=16K head takes the oracle ~2 min
-def test_backward_full_size_one_head(name):
-    # the workload on the GPU (all heads, the benchmark's launch); the oracle checks the gradients
-    # of one head (batch 1 or 0, head 1) in full.
+@pytest.mark.parametrize("name,heads", [("S=4K", (1,)), ("S=8K", (1,)), ("S=16K", (0, 5, 10, 15))])
+def test_backward_full_size_whole_heads(name, heads):
+    # the workload on the GPU (all heads, the benchmark's launch); the oracle checks every
+    # gradient element of the listed heads (of batch 1, or 0 when B == 1).  The oracle runs one
+    # thread per head, so the four S=16K heads take about as long as one (~2-3 min).
     w = wl.ALL[name]
     qb, kb, vb = wl.workload_inputs_bits(w)
     dob = wl.make_inputs_bits(w.B, w.H, w.Sq, w.Sq, 128, seed=77)[0]
@@ -90,9 +91,11 @@ def test_backward_full_size_one_head(name):
     o, lse = attn.fwd(q, k, v, scale=w.scale)
     dq, dk, dv = attn.bwd(q, k, v, o, do, lse, scale=w.scale)
     torch.cuda.synchronize()
-    sl = (slice(min(1, w.B - 1), min(1, w.B - 1) + 1), slice(1, 2))
-    ref = oracle.attn_bwd(qb[sl], kb[sl], vb[sl], dob[sl], w.scale)
-    got = [t[sl].float().cpu().numpy().astype(np.float64) for t in (dq, dk, dv)]
+    b = min(1, w.B - 1)
+    hs = list(heads)
+    pick = lambda x: np.ascontiguousarray(x[b:b + 1][:, hs])
+    ref = oracle.attn_bwd(pick(qb), pick(kb), pick(vb), pick(dob), w.scale)
+    got = [t[b:b + 1][:, hs].float().cpu().numpy().astype(np.float64) for t in (dq, dk, dv)]
     _check(got, ref)
 
 

@@ -1,11 +1,12 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
 
 Tolerances (the stated bar): O max-abs <= 2e-2 and mean-abs <= 2e-3 over the
-compared elements; LSE max-abs <= 1e-3.  Small shapes are compared element by
-element over every output; the full-size workloads, in the exact launch
-configuration the benchmark times, are compared on sampled rows that the
-oracle computes one by one (first/last rows of Q tiles, every work item that
-is the last of its CTA, random rows).
+compared elements; LSE max-abs <= 1e-3.  Small shapes and the full-size
+workloads (in the exact launch configuration the benchmark times) are compared
+element by element over every output; some variants of the full-size launches
+(causal, [B,S,H,D], host buffers) are compared on sampled rows that the oracle
+computes one by one (first/last rows of Q tiles, every work item that is the
+last of its CTA, random rows).
 """
 import math
 
@@ -75,6 +76,53 @@ def test_softmax_stress():
     w = wl.STRESS
     _full_check(w.B, w.H, w.Sq, w.Sk, seed=w.seeds[0], qk_std=w.qk_std,
                 spike_every=w.spike_every, spike_factor=w.spike_factor)
+
+
+@pytest.mark.parametrize("name", ["tiny", "softmax-stress"])
+def test_contract_entry_point_attn_fwd(name):
+    """The entry point with the contracted signature, attn_fwd(q, k, v, o, lse, B, H, Sq, Sk, D,
+    scale, stream), called directly through ctypes on device buffers: every element of O and LSE
+    against the oracle, on a non-default stream."""
+    w = wl.ALL[name]
+    qb, kb, vb = wl.workload_inputs_bits(w)
+    q, k, v = (wl.bits_to_torch(x).cuda() for x in (qb, kb, vb))
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((w.B, w.H, w.Sq), float("nan"), device="cuda")
+    lib = attn.library()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    rc = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                      w.B, w.H, w.Sq, w.Sk, w.D, w.scale, s.cuda_stream)
+    assert rc == attn.ATTN_OK, attn.status_string(rc)
+    s.synchronize()
+    o_ref, lse_ref = oracle.attn_fwd(qb, kb, vb, w.scale)
+    _assert_close(o.float().cpu().numpy().astype(np.float64), o_ref,
+                  lse.cpu().numpy().astype(np.float64), lse_ref)
+    assert attn.device_status() == 0
+
+
+@pytest.mark.parametrize("shape,seed", [
+    ((1, 41, 1100, 6000), 77),   # 6,000 keys, ragged last Q and KV tiles
+    ((1, 16, 1024, 4096), 11),
+])
+def test_stress_logits_long_key_sequences(shape, seed):
+    """Stress logits (Q, K ~ N(0, 3^2), every 64th key x8) over thousands of keys with V ~ N(0, 1),
+    every work item whole in one CTA (attn_fwd_ex), every element against the oracle.  Most rows
+    are dominated by one key whose P, rounded to BF16 for P*V, would differ from the fp32 row sum
+    by up to 2^-8 relative; the kernel carries that rounding of each tile's largest P in the sum
+    it divides O by, so those rows meet the bar (a CPU emulation of the kernel's rounding gives
+    0.016 / 0.015 max-abs on these inputs, 0.025 / 0.017 with the plain fp32 row sum)."""
+    B, H, Sq, Sk = shape
+    qb, kb, vb = wl.make_inputs_bits(B, H, Sq, Sk, 128, seed=seed, qk_std=3.0, spike_every=64,
+                                     spike_factor=8.0)
+    scale = 1.0 / math.sqrt(128)
+    q, k, v = (wl.bits_to_torch(x).cuda() for x in (qb, kb, vb))
+    o, lse = _fwd_whole_items(q, k, v, scale)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.attn_fwd(qb, kb, vb, scale)
+    _assert_close(o.float().cpu().numpy().astype(np.float64), o_ref,
+                  lse.cpu().numpy().astype(np.float64), lse_ref)
+    assert attn.device_status() == 0
 
 
 @pytest.mark.parametrize("shape", [
@@ -226,20 +274,14 @@ def _rows_sample(w, n_random, seed):
 
 
 @pytest.mark.parametrize("name", ["S=4K", "S=8K", "S=16K", "S=12K,H=24"])
-def test_full_size_workload_sampled_rows(name):
+def test_full_size_workload_every_element(name):
+    """The full-size workloads in the launch configuration the benchmark times (attn.fwd, i.e.
+    attn_fwd_ws with its workspace): every element of O and LSE against the oracle."""
     w = wl.ALL[name]
     qb, kb, vb = wl.workload_inputs_bits(w)
     o, lse = _run(qb, kb, vb, w.scale)
-    bh, rows = _rows_sample(w, 400, seed=1)
-    o_ref, lse_ref = oracle.attn_fwd_rows(qb, kb, vb, w.scale, bh, rows)
-    D = w.D
-    _assert_close(o.reshape(-1, w.Sq, D)[bh, rows], o_ref, lse.reshape(-1, w.Sq)[bh, rows], lse_ref)
-    # properties at every row: outputs are convex combinations of V rows
-    v = wl.bf16_bits_to_f32(vb).reshape(-1, w.Sk, D)
-    vmin, vmax = v.min(axis=1), v.max(axis=1)
-    o3 = o.reshape(-1, w.Sq, D)
-    assert (o3 >= vmin[:, None, :] - 1e-2).all() and (o3 <= vmax[:, None, :] + 1e-2).all()
-    assert np.isfinite(lse).all()
+    o_ref, lse_ref = oracle.attn_fwd(qb, kb, vb, w.scale)
+    _assert_close(o, o_ref, lse, lse_ref)
 
 
 # ------------------------------------------------------------- causal (top-left aligned)
@@ -522,17 +564,16 @@ def _split_call(q, k, v, scale, lse=True, workspace="auto"):
 
 def test_split_schedule_stress_logits_ragged_queries_and_no_lse():
     """Split items whose two parts keep very different row maxima (stress logits: Q, K ~ N(0, 3^2)
-    with every 64th key x8), a ragged last Q tile (rows past Sq are not outputs), and the call
-    without an LSE buffer, which must give the same O bitwise.  V ~ N(0, 0.5^2): with 6,000 keys
-    and these logits most rows copy one V row, and with V ~ N(0, 1) the pages' rounding alone (BF16
-    P over an fp32 row sum, BF16 O) reaches 0.025 max-abs on this input for whole items as well (a
-    CPU emulation of that rounding gives 0.0250 whole and 0.0205 split, and 0.0125 / 0.0102 at
-    this V scale)."""
+    with every 64th key x8, V ~ N(0, 1)), a ragged last Q tile (rows past Sq are not outputs), and
+    the call without an LSE buffer, which must give the same O bitwise.  With 6,000 keys most rows
+    copy one V row; O is divided by the row sum of the weights P*V multiplies (the BF16 rounding
+    of each tile's largest P carried in the sum), so such a row's output is that V row up to the
+    final BF16 rounding of O."""
     B, H, Sq, Sk = 1, 41, 1100, 6000
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert _split_items(B, H, Sq, Sk, sms)
     qb, kb, vb = wl.make_inputs_bits(B, H, Sq, Sk, 128, seed=77, qk_std=3.0, spike_every=64,
-                                     spike_factor=8.0, v_std=0.5)
+                                     spike_factor=8.0)
     scale = 1.0 / math.sqrt(128)
     q, k, v = (wl.bits_to_torch(x).cuda() for x in (qb, kb, vb))
     o, lse = _split_call(q, k, v, scale)

@@ -4,10 +4,12 @@ Some callers of this library cannot allocate device memory around it: code runni
 fixed memory budget or its own allocator, embedders that own every device allocation, or paths
 where a cudaMalloc would synchronise the device.  attn_bwd needs a scratch buffer (delta, one
 float per query row) from its caller; attn_bwd_noalloc uses a fixed 4 MiB array compiled into
-the library instead.  This test checks that its gradients agree with attn_bwd's on the same
+the library instead.  These tests check that its gradients agree with attn_bwd's on the same
 inputs, on two calls in a row with different inputs (the array keeps the previous call's
-contents, which must not leak into the next result), and that a problem beyond the array's
-size is rejected.  It runs last (file name) and also passes alone in a fresh process.
+contents, which must not leak into the next result), that calls after the first one on a device
+leave the device's free memory unchanged (also a larger problem after a smaller one), and that
+a problem beyond the array's size is rejected.  The file runs last (its name) and also passes
+alone in a fresh process.
 """
 import ctypes
 import math
@@ -28,8 +30,9 @@ def lib():
     return attn.library()
 
 
-def _noalloc(lib, q, k, v, o, do, lse, scale, causal):
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+def _noalloc(lib, q, k, v, o, do, lse, scale, causal, out=None):
+    dq, dk, dv = out if out is not None else (torch.empty_like(q), torch.empty_like(k),
+                                              torch.empty_like(v))
     B, H, Sq, D = q.shape
     rc = lib.attn_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
                               lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Sq,
@@ -63,6 +66,38 @@ def test_noalloc_backward_matches_attn_bwd_on_two_calls(lib):
         got = _noalloc(lib, q, k, v, o, do, lse, scale, causal)
         torch.cuda.synchronize()
         _close(got, ref)
+    assert attn.device_status() == 0
+
+
+def _problem(B, H, Sq, Sk, seed, causal=False):
+    qb, kb, vb = wl.make_inputs_bits(B, H, Sq, Sk, 128, seed=seed)
+    dob = wl.make_inputs_bits(B, H, Sq, Sq, 128, seed=seed + 1)[0]
+    q, k, v, do = (wl.bits_to_torch(x).cuda() for x in (qb, kb, vb, dob))
+    scale = 1.0 / math.sqrt(128)
+    o, lse = attn.fwd(q, k, v, scale=scale, causal=causal)
+    ref = attn.bwd(q, k, v, o, do, lse, scale=scale, causal=causal)
+    out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    return (q, k, v, o, do, lse, scale, causal), ref, out
+
+
+def test_noalloc_call_allocates_no_device_memory(lib):
+    """After the first call on the device (its one-time set-up), calls change the device's free
+    memory by nothing, also when a larger problem follows a smaller one; the larger one's
+    gradients still agree with attn_bwd's.  Every buffer, including attn_bwd's reference results,
+    is allocated before the measured calls."""
+    attn.device_status(clear=True)
+    small, ref_small, out_small = _problem(1, 2, 256, 384, seed=81)
+    large, ref_large, out_large = _problem(4, 16, 1024, 1024, seed=83, causal=True)   # 64K rows
+    _noalloc(lib, *small, out=out_small)   # the first call on this device may set things up
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    _noalloc(lib, *small, out=out_small)
+    _noalloc(lib, *large, out=out_large)
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    assert free1 == free0, f"device free memory changed by {free0 - free1} bytes"
+    _close(out_small, ref_small)
+    _close(out_large, ref_large)
     assert attn.device_status() == 0
 
 
