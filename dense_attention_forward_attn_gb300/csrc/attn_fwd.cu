@@ -419,6 +419,7 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
   p.causal = (flags & ATTN_FLAG_CAUSAL) ? 1 : 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   p.test_withhold = (flags & ATTN_FLAG_TEST_WITHHOLD) ? 1 : 0;
+  p.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0 ? 1 : 0;
   const int grid = p.num_items < info.num_sms ? p.num_items : info.num_sms;
   p.sk_item0 = p.num_items;
   p.sk_items = 0;

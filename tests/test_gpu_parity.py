@@ -229,6 +229,24 @@ def test_run_to_run_bitwise_deterministic():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+def test_output_aligned_to_16_bytes_only():
+    """An output buffer that is 16- but not 32-byte aligned (the stated minimum) takes the
+    epilogue's 16-byte stores; the result is bitwise the one written to an aligned buffer."""
+    qb, kb, vb = wl.make_inputs_bits(2, 3, 384, 640, 128, seed=13)
+    q, k, v = (wl.bits_to_torch(x).cuda() for x in (qb, kb, vb))
+    o_ref, lse_ref = _fwd_whole_items(q, k, v, 0.09)
+    raw = torch.zeros(q.numel() * 2 + 64, dtype=torch.uint8, device="cuda")
+    base = raw.data_ptr()
+    off = (32 - base % 32) % 32 + 16            # 16 mod 32
+    o = raw[off:off + q.numel() * 2].view(torch.bfloat16).view(q.shape)
+    assert o.data_ptr() % 32 == 16
+    lse = torch.empty_like(lse_ref)
+    attn.fwd_into(q, k, v, o, lse, 0.09)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+    assert bool((raw[:off] == 0).all()) and bool((raw[off + q.numel() * 2:] == 0).all())
+
+
 def test_lse_optional_and_host_buffers():
     qb, kb, vb = wl.make_inputs_bits(1, 2, 256, 256, 128, seed=9)
     q, k, v = (wl.bits_to_torch(x) for x in (qb, kb, vb))
