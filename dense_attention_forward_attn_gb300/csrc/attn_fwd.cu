@@ -60,12 +60,16 @@ int device_info(int dev, DeviceInfo* out) {
   };
   if (!d.attr_set) {
     const void* fwd_kernels[] = {
-        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false>),
-        reinterpret_cast<const void*>(attn::attn_fwd_kernel<true, false, false>),
-        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, false>),
-        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, true>),
-        reinterpret_cast<const void*>(attn::attn_fwd_kernel<true, false, true>),
-        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, true>)};
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, true>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, false>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<true, false, false, true>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, false, true>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, false, false>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, true, true>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, true, false>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<true, false, true, true>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, true, true>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, true, false>)};
     for (const void* fn : fwd_kernels) {
       if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(attn::kSmemBytes)) != cudaSuccess) {
@@ -445,20 +449,26 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
     p.seq = next_seq();
   }
 
-  // Instantiations: <software exp2, split schedule, [B,S,H,D]>; the split schedule is never
-  // used with the software exp2.
+  // Instantiations: <software exp2, split schedule, [B,S,H,D], maskable>; the split schedule is
+  // never used with the software exp2, which is built maskable only.  A launch needs the masking
+  // code only with a ragged last key tile, the causal mask or a zero scale.
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const bool soft = (flags & ATTN_FLAG_SOFT_EXP2) != 0;
-#define ATTN_LAUNCH(S, P, L) \
-  attn::attn_fwd_kernel<S, P, L><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tm_q, tm_k, tm_v, p)
+  const bool mask = p.causal != 0 || p.kv_valid_last != attn::kBlockN || p.scale_log2 == 0.f;
+#define ATTN_LAUNCH(S, P, L, M) \
+  attn::attn_fwd_kernel<S, P, L, M><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tm_q, tm_k, tm_v, p)
   if (bshd) {
-    if (sp.on) ATTN_LAUNCH(false, true, true);
-    else if (soft) ATTN_LAUNCH(true, false, true);
-    else ATTN_LAUNCH(false, false, true);
+    if (soft) ATTN_LAUNCH(true, false, true, true);
+    else if (sp.on && mask) ATTN_LAUNCH(false, true, true, true);
+    else if (sp.on) ATTN_LAUNCH(false, true, true, false);
+    else if (mask) ATTN_LAUNCH(false, false, true, true);
+    else ATTN_LAUNCH(false, false, true, false);
   } else {
-    if (sp.on) ATTN_LAUNCH(false, true, false);
-    else if (soft) ATTN_LAUNCH(true, false, false);
-    else ATTN_LAUNCH(false, false, false);
+    if (soft) ATTN_LAUNCH(true, false, false, true);
+    else if (sp.on && mask) ATTN_LAUNCH(false, true, false, true);
+    else if (sp.on) ATTN_LAUNCH(false, true, false, false);
+    else if (mask) ATTN_LAUNCH(false, false, false, true);
+    else ATTN_LAUNCH(false, false, false, false);
   }
 #undef ATTN_LAUNCH
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;

@@ -900,7 +900,7 @@ __device__ __noinline__ bool epilogue_split(const Ctx& c, const SplitOut p, int 
   return true;
 }
 
-template <bool kSoftExp2, bool kSplit>
+template <bool kSoftExp2, bool kSplit, bool kMaskable>
 __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int q) {
   SmemCtl* ctl = c.ctl;
   const uint32_t row_base = 32u * (c.warp & 3u);
@@ -952,7 +952,11 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
       // tile.  They must not enter the max and get P = 0 below.  The test is warp-uniform.
       const int jg = sg.j0 + j;   // KV tile index within the head
       const bool diag = p.causal != 0 && jg == qtile;
-      const bool partial = zero_scale || diag || (jg == p.kv_tiles - 1 && p.kv_valid_last < kBlockN);
+      // kMaskable: the launch may have masked columns (a ragged last key tile, the causal diagonal
+      // or a zero scale).  The instantiation for launches without any has no masking code: its
+      // presence, never taken, cost the dense forward ~2% (same-box A/B, bitwise the same).
+      const bool partial =
+          kMaskable && (zero_scale || diag || (jg == p.kv_tiles - 1 && p.kv_valid_last < kBlockN));
       int valid = kBlockN;
       if (jg == p.kv_tiles - 1) valid = p.kv_valid_last;
       if (diag) valid = min(valid, row + 1);
@@ -1045,7 +1049,7 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
 }
 
 // ------------------------------------------------------------------ kernel
-template <bool kSoftExp2, bool kSplit, bool kBshd>
+template <bool kSoftExp2, bool kSplit, bool kBshd, bool kMaskable>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -1098,7 +1102,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (threadIdx.x == 0) atomicOr(&g_attn_status, kStatusTmemBase);
   } else if (c.warp < kCorrWarp0) {
     ptx::setmaxnreg_inc<kRegSoftmax>();
-    softmax_role<kSoftExp2, kSplit>(c, p, static_cast<int>(c.warp >> 2));
+    softmax_role<kSoftExp2, kSplit, kMaskable>(c, p, static_cast<int>(c.warp >> 2));
   } else if (c.warp < kLoadWarp) {
     ptx::setmaxnreg_dec<kRegCorr>();
     correction_role<kSplit>(c, p);
