@@ -317,7 +317,7 @@ struct Ctx {
   // Warp-uniform bounded wait; all 32 lanes call it.  false = timed out or aborted.
   __device__ bool wait(const uint64_t& b, uint32_t parity, unsigned role_bit) const {
     const uint32_t addr = bar(b);
-    if (__all_sync(0xffffffffu, ptx::mbar_try_wait(addr, parity))) return true;
+    if (__builtin_expect(__all_sync(0xffffffffu, ptx::mbar_try_wait(addr, parity)), 1)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     while (true) {
       if (__all_sync(0xffffffffu, ptx::mbar_try_wait(addr, parity))) return true;
@@ -337,6 +337,11 @@ struct Ctx {
   __device__ bool wait2(const uint64_t& b1, uint32_t par1, const uint64_t& b2, uint32_t par2,
                         unsigned role_bit) const {
     const uint32_t a1 = bar(b1), a2 = bar(b2);
+    {
+      const uint32_t r1 = ptx::mbar_try_wait(a1, par1);
+      const uint32_t r2 = ptx::mbar_try_wait(a2, par2);
+      if (__builtin_expect(__all_sync(0xffffffffu, r1 & r2), 1)) return true;
+    }
     const uint64_t t0 = ptx::globaltimer_ns();
     while (true) {
       const uint32_t r1 = ptx::mbar_try_wait(a1, par1);
@@ -407,7 +412,7 @@ __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const C
   bool withhold = p.test_withhold != 0 && blockIdx.x == 0;
   auto load_kv = [&](const CUtensorMap* tm, int bh, int row) -> bool {
     if (!c.wait(ctl->kv_empty[slot], phase ^ 1u, kStatusTimeoutLoad)) return false;
-    if (withhold) {   // the slot is skipped: nothing is loaded into it, nothing to drain
+    if (__builtin_expect(withhold, 0)) {   // the slot is skipped: nothing is loaded into it, nothing to drain
       withhold = false;
       if (++slot == kKvStages) { slot = 0; phase ^= 1u; }
       return true;
@@ -758,7 +763,7 @@ __device__ __forceinline__ void epilogue_store(const Params& p, int q, const Wor
   const int b = w.bh / p.heads, h = w.bh - b * p.heads;
   uint8_t* out = static_cast<uint8_t*>(p.o) +
                  (b * p.o_batch_stride + h * p.o_head_stride + grow * p.o_row_stride) * 2;
-  if (p.o_align32) {   // 32-byte stores where the output allows them
+  if (__builtin_expect(p.o_align32, 1)) {   // 32-byte stores where the output allows them
 #pragma unroll
     for (int i = 0; i < 8; ++i) ptx::st_global_v8(out + 32 * i, pk + 8 * i);
   } else {
@@ -968,7 +973,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
       float alpha = 1.f;
       if (j == 0) {
         m_kept = m_tile;
-      } else if (m_tile - m_kept >= kRebaseThresholdLog2) {
+      } else if (__builtin_expect(m_tile - m_kept >= kRebaseThresholdLog2, 0)) {
         alpha = ptx::ex2_ftz(m_kept - m_tile);
         l *= alpha;
         dl *= alpha;
@@ -1026,7 +1031,7 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
         // alpha is 1 on an item's first tile, so the previous item's O, which its softmax
         // warpgroup may still be reading, is not touched here.
         const float a = ctl->alpha[q][tphase[q]][row];
-        if (__any_sync(0xffffffffu, a != 1.0f)) {
+        if (__builtin_expect(__any_sync(0xffffffffu, a != 1.0f), 0)) {
           const uint32_t taddr_o = c.tmem + (row_base << 16) + col_o(q);
           ptx::tc_fence_after();
 #pragma unroll 1
