@@ -406,6 +406,9 @@ __device__ __forceinline__ void dq_loads(const Layout& L, const Sync& s, const C
   if (nkv > 0) s.drain_wait(ctl->dq_do_full, 0);
 }
 
+// kMask: the launch may have masked keys (a ragged last K/V tile or the causal mask); the
+// instantiation for launches without any has no masking code.
+template <bool kMask>
 __global__ void __launch_bounds__(kDqThreads, 1)
 attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -529,8 +532,10 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       ptx::tc_fence_before();
       s.arrive(ctl->dq_x_read[t]);   // dP_t may now overwrite S_t
       int valid = kBlockN;
-      if (j == p.kv_tiles - 1) valid = p.kv_valid_last;
-      if (p.causal && j == qt) valid = min(valid, r + 1);
+      if (kMask) {
+        if (j == p.kv_tiles - 1) valid = p.kv_valid_last;
+        if (p.causal && j == qt) valid = min(valid, r + 1);
+      }
       // P = exp2(S * scale_log2 - LSE * log2 e), 0 past `valid`; kept in fp32 for dS.
       float2 pf[4][16];
       const float2 sl2 = make_float2(p.scale_log2, p.scale_log2), nl = make_float2(-lse2, -lse2);
@@ -540,8 +545,8 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         for (int i = 0; i < 16; ++i) {
           const float2 e = ptx::ffma2(
               make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), sl2, nl);
-          pf[c][i].x = 32 * c + 2 * i < valid ? ptx::ex2_ftz(e.x) : 0.f;
-          pf[c][i].y = 32 * c + 2 * i + 1 < valid ? ptx::ex2_ftz(e.y) : 0.f;
+          pf[c][i].x = (!kMask || 32 * c + 2 * i < valid) ? ptx::ex2_ftz(e.x) : 0.f;
+          pf[c][i].y = (!kMask || 32 * c + 2 * i + 1 < valid) ? ptx::ex2_ftz(e.y) : 0.f;
         }
       }
       // dS = P o (dP - delta), packed BF16 into columns 16c..16c+15 once dP columns
@@ -614,6 +619,8 @@ __device__ __forceinline__ void dkdv_item(const Params& p, int& bh, int& kt, int
   }
 }
 
+// kMask: the launch uses the causal mask (the only per-element masking this kernel does).
+template <bool kMask>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -750,7 +757,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       if (!(ok = s.wait(ctl->vec_sync, par, kStatusTimeoutSoftmax))) break;
       if (!(ok = s.wait(ctl->s_full, par, kStatusTimeoutSoftmax))) break;
       ptx::tc_fence_after();
-      const bool diag = p.causal && q0 + i == kt;   // query column c < key row r is masked
+      const bool diag = kMask && p.causal && q0 + i == kt;   // query column c < key row r is masked
       const float* va = ctl->lse2[par] + c0;
       const float* vd = ctl->dlt[par] + c0;
       // P^T = exp2(S^T * scale_log2 + (-LSE_col * log2 e)), kept in fp32 for dS^T.  The packed

@@ -84,18 +84,28 @@ int device_info(int dev, DeviceInfo* out) {
     d.attr_set = true;
   }
   if (!d.bwd_attr_set) {
-    if (cudaFuncSetAttribute(attn::bwd::attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(attn::bwd::kSmemBytesDq)) != cudaSuccess ||
-        cudaFuncSetAttribute(attn::bwd::attn_bwd_dkdv_kernel,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(attn::bwd::kSmemBytesDkdv)) != cudaSuccess) {
-      cudaGetLastError();
-      return ATTN_ERR_CUDA;
+    const void* dq_kernels[] = {reinterpret_cast<const void*>(attn::bwd::attn_bwd_dq_kernel<true>),
+                                reinterpret_cast<const void*>(attn::bwd::attn_bwd_dq_kernel<false>)};
+    const void* dkdv_kernels[] = {
+        reinterpret_cast<const void*>(attn::bwd::attn_bwd_dkdv_kernel<true>),
+        reinterpret_cast<const void*>(attn::bwd::attn_bwd_dkdv_kernel<false>)};
+    for (const void* fn : dq_kernels) {
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(attn::bwd::kSmemBytesDq)) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+      }
+      if (!regs_are(fn, static_cast<int>(attn::bwd::kDqRegLaunch))) {
+        cudaGetLastError();
+        return ATTN_ERR_UNSUPPORTED;
+      }
     }
-    if (!regs_are(reinterpret_cast<const void*>(attn::bwd::attn_bwd_dq_kernel),
-                  static_cast<int>(attn::bwd::kDqRegLaunch))) {
-      cudaGetLastError();
-      return ATTN_ERR_UNSUPPORTED;
+    for (const void* fn : dkdv_kernels) {
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(attn::bwd::kSmemBytesDkdv)) != cudaSuccess) {
+        cudaGetLastError();
+        return ATTN_ERR_CUDA;
+      }
     }
     d.bwd_attr_set = true;
   }
@@ -758,14 +768,27 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   }
   p.out0 = dk;
   p.out1 = dv;
-  attn::bwd::attn_bwd_dkdv_kernel<<<static_cast<unsigned>(bh * p.kv_tiles), attn::bwd::kThreads,
-                                    attn::bwd::kSmemBytesDkdv, st>>>(tm_q, tm_k, tm_v, tm_do,
-                                                                      tm_dk, tm_dv, p);
+  // The masking code is compiled only into the instantiations for launches that need it (the
+  // causal mask; for the dQ kernel also a ragged last K/V tile).
+  const bool mask_dq = p.causal != 0 || p.kv_valid_last != attn::kBlockN;
+  if (p.causal)
+    attn::bwd::attn_bwd_dkdv_kernel<true><<<static_cast<unsigned>(bh * p.kv_tiles), attn::bwd::kThreads,
+                                            attn::bwd::kSmemBytesDkdv, st>>>(tm_q, tm_k, tm_v, tm_do,
+                                                                              tm_dk, tm_dv, p);
+  else
+    attn::bwd::attn_bwd_dkdv_kernel<false><<<static_cast<unsigned>(bh * p.kv_tiles), attn::bwd::kThreads,
+                                             attn::bwd::kSmemBytesDkdv, st>>>(tm_q, tm_k, tm_v, tm_do,
+                                                                               tm_dk, tm_dv, p);
   p.out0 = dq;
   p.out1 = nullptr;
-  attn::bwd::attn_bwd_dq_kernel<<<static_cast<unsigned>(bh * ((p.q_tiles + 1) / 2)),
-                                  attn::bwd::kDqThreads, attn::bwd::kSmemBytesDq, F.side>>>(
-      tm_q, tm_k, tm_v, tm_do, p);
+  if (mask_dq)
+    attn::bwd::attn_bwd_dq_kernel<true><<<static_cast<unsigned>(bh * ((p.q_tiles + 1) / 2)),
+                                          attn::bwd::kDqThreads, attn::bwd::kSmemBytesDq, F.side>>>(
+        tm_q, tm_k, tm_v, tm_do, p);
+  else
+    attn::bwd::attn_bwd_dq_kernel<false><<<static_cast<unsigned>(bh * ((p.q_tiles + 1) / 2)),
+                                           attn::bwd::kDqThreads, attn::bwd::kSmemBytesDq, F.side>>>(
+        tm_q, tm_k, tm_v, tm_do, p);
   const bool launched = cudaGetLastError() == cudaSuccess;
   // Join even after a failed launch, so the caller's stream never runs ahead of a dQ in flight.
   if (cudaEventRecord(F.join, F.side) != cudaSuccess || cudaStreamWaitEvent(st, F.join, 0) != cudaSuccess) {
