@@ -406,6 +406,23 @@ __device__ __forceinline__ void dq_loads(const Layout& L, const Sync& s, const C
   if (nkv > 0) s.drain_wait(ctl->dq_do_full, 0);
 }
 
+// P of one S row (128 columns) for the dQ kernel: exp2(S * scale_log2 - LSE * log2 e), with
+// kSel, 0 at columns >= valid.
+template <bool kSel>
+__device__ __forceinline__ void dq_p(const uint32_t (&sr)[4][32], float2 sl2, float2 nl, int valid,
+                                     float2 (&pf)[4][16]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 e = ptx::ffma2(
+          make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), sl2, nl);
+      pf[c][i].x = (!kSel || 32 * c + 2 * i < valid) ? ptx::ex2_ftz(e.x) : 0.f;
+      pf[c][i].y = (!kSel || 32 * c + 2 * i + 1 < valid) ? ptx::ex2_ftz(e.y) : 0.f;
+    }
+  }
+}
+
 // kMask: the launch may have masked keys (a ragged last K/V tile or the causal mask); the
 // instantiation for launches without any has no masking code.
 template <bool kMask>
@@ -531,23 +548,18 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       ptx::tmem_wait_ld();
       ptx::tc_fence_before();
       s.arrive(ctl->dq_x_read[t]);   // dP_t may now overwrite S_t
-      int valid = kBlockN;
-      if (kMask) {
-        if (j == p.kv_tiles - 1) valid = p.kv_valid_last;
-        if (p.causal && j == qt) valid = min(valid, r + 1);
-      }
-      // P = exp2(S * scale_log2 - LSE * log2 e), 0 past `valid`; kept in fp32 for dS.
+      // P = exp2(S * scale_log2 - LSE * log2 e), 0 past `valid`; kept in fp32 for dS.  Only the
+      // tiles with masked keys (the ragged last one, the causal diagonal) take the selects.
       float2 pf[4][16];
       const float2 sl2 = make_float2(p.scale_log2, p.scale_log2), nl = make_float2(-lse2, -lse2);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 e = ptx::ffma2(
-              make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), sl2, nl);
-          pf[c][i].x = (!kMask || 32 * c + 2 * i < valid) ? ptx::ex2_ftz(e.x) : 0.f;
-          pf[c][i].y = (!kMask || 32 * c + 2 * i + 1 < valid) ? ptx::ex2_ftz(e.y) : 0.f;
-        }
+      const bool masked_tile = kMask && ((j == p.kv_tiles - 1 && p.kv_valid_last < kBlockN) ||
+                                         (p.causal && j == qt));
+      if (masked_tile) {
+        int valid = j == p.kv_tiles - 1 ? p.kv_valid_last : kBlockN;
+        if (p.causal && j == qt) valid = min(valid, r + 1);
+        dq_p<true>(sr, sl2, nl, valid, pf);
+      } else {
+        dq_p<false>(sr, sl2, nl, kBlockN, pf);
       }
       // dS = P o (dP - delta), packed BF16 into columns 16c..16c+15 once dP columns
       // 32c..32c+31 are in registers: every column written has been read.  The load of the
@@ -616,6 +628,30 @@ __device__ __forceinline__ void dkdv_item(const Params& p, int& bh, int& kt, int
     kt = static_cast<int>(blockIdx.x) % p.kv_tiles;
     q0 = 0;
     nq = p.q_tiles;
+  }
+}
+
+// P^T of 64 columns (query columns c0..c0+63 of key row r) for the dK/dV kernel: exp2(S^T *
+// scale_log2 - LSE_col * log2 e); with kDiag, 0 at query columns c < r (the causal diagonal).
+template <bool kDiag>
+__device__ __forceinline__ void dkdv_p(const uint32_t (&xr)[2][32], const float* va, float2 sl2,
+                                       int c0, int r, float2 (&pf)[2][16]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int i2 = 0; i2 < 16; ++i2) {
+      const int col = c0 + 32 * h + 2 * i2;
+      const float2 a = *reinterpret_cast<const float2*>(va + 32 * h + 2 * i2);
+      const float2 e = ptx::ffma2(make_float2(__uint_as_float(xr[h][2 * i2]),
+                                              __uint_as_float(xr[h][2 * i2 + 1])), sl2, a);
+      float p0 = ptx::ex2_ftz(e.x);
+      float p1 = ptx::ex2_ftz(e.y);
+      if (kDiag) {
+        p0 = col < r ? 0.f : p0;
+        p1 = col + 1 < r ? 0.f : p1;
+      }
+      pf[h][i2] = make_float2(p0, p1);
+    }
   }
 }
 
@@ -769,23 +805,8 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       ptx::tmem_wait_ld_regs(xr[0]);
       ptx::tmem_wait_ld_regs(xr[1]);
       float2 pf[2][16];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-#pragma unroll
-        for (int i2 = 0; i2 < 16; ++i2) {
-          const int col = c0 + 32 * h + 2 * i2;
-          const float2 a = *reinterpret_cast<const float2*>(va + 32 * h + 2 * i2);
-          const float2 e = ptx::ffma2(make_float2(__uint_as_float(xr[h][2 * i2]),
-                                                  __uint_as_float(xr[h][2 * i2 + 1])), sl2, a);
-          float p0 = ptx::ex2_ftz(e.x);
-          float p1 = ptx::ex2_ftz(e.y);
-          if (diag) {
-            p0 = col < r ? 0.f : p0;
-            p1 = col + 1 < r ? 0.f : p1;
-          }
-          pf[h][i2] = make_float2(p0, p1);
-        }
-      }
+      if (diag) dkdv_p<true>(xr, va, sl2, c0, r, pf);   // only the causal diagonal tile selects
+      else dkdv_p<false>(xr, va, sl2, c0, r, pf);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t pp[16];
