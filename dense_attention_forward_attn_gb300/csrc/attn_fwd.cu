@@ -464,7 +464,8 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
   // code only with a ragged last key tile, the causal mask or a zero scale.
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const bool soft = (flags & ATTN_FLAG_SOFT_EXP2) != 0;
-  const bool mask = p.causal != 0 || p.kv_valid_last != attn::kBlockN || p.scale_log2 == 0.f;
+  const bool mask = p.causal != 0 || p.kv_valid_last != attn::kBlockN || p.scale_log2 == 0.f ||
+                    Sq % (2 * attn::kBlockM) != 0 || !p.o_align32 || p.test_withhold;
 #define ATTN_LAUNCH(S, P, L, M) \
   attn::attn_fwd_kernel<S, P, L, M><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tm_q, tm_k, tm_v, p)
   if (bshd) {

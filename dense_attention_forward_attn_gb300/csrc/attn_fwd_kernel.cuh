@@ -375,7 +375,7 @@ struct Ctx {
 // ------------------------------------------------------------------ TMA warp
 // kBshd: the layout is a template parameter, so each instantiation's TMA warp holds only its own
 // tensor-map rank (a run-time layout branch in the box loads measured up to 3% slower).
-template <bool kSplit, bool kBshd>
+template <bool kSplit, bool kBshd, bool kMaskable>
 __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const CUtensorMap* tm_q,
                                           const CUtensorMap* tm_k, const CUtensorMap* tm_v) {
   SmemCtl* ctl = c.ctl;
@@ -409,7 +409,8 @@ __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const C
       ptx::tma_prefetch_3d(tm, 64, row, bh);
     }
   };
-  bool withhold = p.test_withhold != 0 && blockIdx.x == 0;
+  // (the test hook exists in the maskable instantiations only; the host sends its launches there)
+  bool withhold = kMaskable && p.test_withhold != 0 && blockIdx.x == 0;
   auto load_kv = [&](const CUtensorMap* tm, int bh, int row) -> bool {
     if (!c.wait(ctl->kv_empty[slot], phase ^ 1u, kStatusTimeoutLoad)) return false;
     if (__builtin_expect(withhold, 0)) {   // the slot is skipped: nothing is loaded into it, nothing to drain
@@ -504,8 +505,11 @@ __device__ __forceinline__ void issue_pv(const Ctx& c, int vslot, bool overwrite
   }
 }
 
-template <bool kSplit>
+template <bool kSplit, bool kMaskable>
 __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
+  // The instantiation without masking runs only launches whose work items all have two Q tiles
+  // over the same KV tiles (dense, an even number of full Q tiles), so both stages have n tiles.
+  constexpr bool kEq = !kMaskable;
   SmemCtl* ctl = c.ctl;
   const bool leader = ptx::elect_one();
   int slot = 0;
@@ -570,6 +574,7 @@ __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
     if (ok && w.n[1] > 0) ok = qk(1, kslot, true, w.n[1] == 1, true);
     while (ok) {
       const int ntiles = w.n[1] > 0 ? w.n[1] : w.n[0];
+      const int n0 = kEq ? ntiles : w.n[0], n1 = kEq ? ntiles : w.n[1];
       Seg nsg;
       const bool has_next = seg_of<kSplit>(r + 1, p, ctl->sk_range, nsg);
       const WorkItem nw = has_next ? nsg.w : w;
@@ -588,34 +593,34 @@ __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
         if (++slot == kKvStages) { slot = 0; phase ^= 1u; }
         int kslot_next = -1;
         // stage 0: P0 V(j), then Q0 K(j+1)
-        if (j < w.n[0]) {
+        if (j < n0) {
           if (!(ok = pv(0, vslot, j == 0, v_phase))) break;
           v_phase = -1;
           if (leader) {
-            if (j == w.n[0] - 1) ptx::mma_commit(c.bar(ctl->o_full[0]));
-            if (j >= w.n[1]) ptx::mma_commit(c.bar(ctl->kv_empty[vslot]));
+            if (j == n0 - 1) ptx::mma_commit(c.bar(ctl->o_full[0]));
+            if (j >= n1) ptx::mma_commit(c.bar(ctl->kv_empty[vslot]));
           }
           __syncwarp();
-          if (j + 1 < w.n[0]) {
+          if (j + 1 < n0) {
             if (!(ok = next_kv(kslot_next))) break;
-            if (!(ok = qk(0, kslot_next, false, j + 1 == w.n[0] - 1, j + 1 >= w.n[1]))) break;
+            if (!(ok = qk(0, kslot_next, false, j + 1 == n0 - 1, j + 1 >= n1))) break;
           } else if (j == ntiles - 1) {
             if (!(ok = issue_next(0))) break;
             next0_done = true;
           }
         }
         // stage 1: P1 V(j), then Q1 K(j+1)
-        if (j < w.n[1]) {
+        if (j < n1) {
           if (!(ok = pv(1, vslot, j == 0, v_phase))) break;
           v_phase = -1;
           if (leader) {
-            if (j == w.n[1] - 1) ptx::mma_commit(c.bar(ctl->o_full[1]));
+            if (j == n1 - 1) ptx::mma_commit(c.bar(ctl->o_full[1]));
             ptx::mma_commit(c.bar(ctl->kv_empty[vslot]));
           }
           __syncwarp();
-          if (j + 1 < w.n[1]) {
+          if (j + 1 < n1) {
             if (kslot_next < 0 && !(ok = next_kv(kslot_next))) break;
-            if (!(ok = qk(1, kslot_next, false, j + 1 == w.n[1] - 1, true))) break;
+            if (!(ok = qk(1, kslot_next, false, j + 1 == n1 - 1, true))) break;
           }
         }
       }
@@ -756,14 +761,15 @@ __device__ __forceinline__ bool epilogue_read(const Ctx& c, int q, uint32_t o_pa
 // are computed but not stored).  The row (256 bytes) goes out in 32-byte stores when the output
 // is 32-byte aligned (half the store instructions of 16-byte ones: measured +1.2% at S=4K and
 // +2.8% causal, where item boundaries are frequent), else in 16-byte stores.  LSE = (kept max + log2 l) * ln 2, l the row sum of the fp32 P.
+template <bool kMaskable>
 __device__ __forceinline__ void epilogue_store(const Params& p, int q, const WorkItem& w, int row,
                                                float m, float l, const uint32_t (&pk)[64]) {
   const int grow = (w.qt0 + q) * kBlockM + row;
-  if (grow >= p.sq) return;
+  if (kMaskable && grow >= p.sq) return;   // (no ragged Q rows in the other instantiations)
   const int b = w.bh / p.heads, h = w.bh - b * p.heads;
   uint8_t* out = static_cast<uint8_t*>(p.o) +
                  (b * p.o_batch_stride + h * p.o_head_stride + grow * p.o_row_stride) * 2;
-  if (__builtin_expect(p.o_align32, 1)) {   // 32-byte stores where the output allows them
+  if (!kMaskable || __builtin_expect(p.o_align32, 1)) {   // 32-byte stores where allowed
 #pragma unroll
     for (int i = 0; i < 8; ++i) ptx::st_global_v8(out + 32 * i, pk + 8 * i);
   } else {
@@ -938,7 +944,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
       } else {
         uint32_t pk[64];
         if (!epilogue_read(c, q, o_parity, 1.0f / lr_prev, pk)) return;
-        epilogue_store(p, q, sp.w, row, m_prev, l_prev, pk);
+        epilogue_store<kMaskable>(p, q, sp.w, row, m_prev, l_prev, pk);
       }
       o_parity ^= 1u;
     }
@@ -1003,7 +1009,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
     } else {
       uint32_t pk[64];
       if (!epilogue_read(c, q, o_parity, 1.0f / lr_prev, pk)) return;
-      epilogue_store(p, q, sp.w, row, m_prev, l_prev, pk);
+      epilogue_store<kMaskable>(p, q, sp.w, row, m_prev, l_prev, pk);
     }
   }
 }
@@ -1113,8 +1119,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     correction_role<kSplit>(c, p);
   } else {
     ptx::setmaxnreg_dec<kRegMisc>();
-    if (c.warp == kLoadWarp) load_role<kSplit, kBshd>(c, p, &tm_q, &tm_k, &tm_v);
-    else if (c.warp == kMmaWarp) mma_role<kSplit>(c, p);
+    if (c.warp == kLoadWarp) load_role<kSplit, kBshd, kMaskable>(c, p, &tm_q, &tm_k, &tm_v);
+    else if (c.warp == kMmaWarp) mma_role<kSplit, kMaskable>(c, p);
   }
 
   ptx::tc_fence_before();
