@@ -457,7 +457,7 @@ __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const C
     }
 #endif
     ok = load_q(0, w.bh, row0) && load_kv(tm_k, w.bh, kv0);
-    if (ok && w.n[1] > 0) ok = load_q(1, w.bh, row0 + kBlockM);
+    if (ok && (!kMaskable || w.n[1] > 0)) ok = load_q(1, w.bh, row0 + kBlockM);
     if (ok) ok = load_kv(tm_v, w.bh, kv0);
     for (int j = 1; ok && j < ntiles; ++j) {
 #if ATTN_L2_PREFETCH > 0
@@ -919,7 +919,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
   const uint32_t taddr_s = c.tmem + (row_base << 16) + col_s(q);
   // A zero scale makes every kept score 0 (mask_scores on every tile) and uses multiplier 1, so
   // masked columns still give -inf * 1 = -inf rather than -inf * 0 = NaN.
-  const bool zero_scale = p.scale_log2 == 0.f;
+  const bool zero_scale = kMaskable && p.scale_log2 == 0.f;
   const float scale_log2 = zero_scale ? 1.f : p.scale_log2;
   const uint32_t keep = zero_scale ? 0u : 0xffffffffu;
   uint32_t tphase = 0;
@@ -933,7 +933,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
     if (!seg_of<kSplit>(r, p, ctl->sk_range, sg)) break;
     const WorkItem& w = sg.w;
     const int ntiles = w.n[q];
-    if (ntiles == 0) continue;
+    if (kMaskable && ntiles == 0) continue;
     const int qtile = w.qt0 + q;
     // The previous item's epilogue, before this item's first P: its O columns are then free
     // when that P is published (the first P*V of an item overwrites O), and the read overlaps
@@ -1017,7 +1017,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
 // ------------------------------------------------------------------ correction warpgroup
 // Per KV tile and stage: if any row of the warp rebased its max, O_q *= alpha in TMEM; then O_q
 // is safe for the next P*V (p_full, together with the softmax's P).
-template <bool kSplit>
+template <bool kSplit, bool kMaskable>
 __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
   SmemCtl* ctl = c.ctl;
   const uint32_t row_base = 32u * (c.warp & 3u);
@@ -1032,7 +1032,7 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
     for (int j = 0; j < ntiles; ++j) {
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        if (j >= w.n[q]) continue;
+        if (kMaskable && j >= w.n[q]) continue;
         if (!c.wait(ctl->stats_full[q], tphase[q], kStatusTimeoutCorrection)) return;
         // alpha is 1 on an item's first tile, so the previous item's O, which its softmax
         // warpgroup may still be reading, is not touched here.
@@ -1116,7 +1116,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     softmax_role<kSoftExp2, kSplit, kMaskable>(c, p, static_cast<int>(c.warp >> 2));
   } else if (c.warp < kLoadWarp) {
     ptx::setmaxnreg_dec<kRegCorr>();
-    correction_role<kSplit>(c, p);
+    correction_role<kSplit, kMaskable>(c, p);
   } else {
     ptx::setmaxnreg_dec<kRegMisc>();
     if (c.warp == kLoadWarp) load_role<kSplit, kBshd, kMaskable>(c, p, &tm_q, &tm_k, &tm_v);
