@@ -60,16 +60,18 @@ int device_info(int dev, DeviceInfo* out) {
   };
   if (!d.attr_set) {
     const void* fwd_kernels[] = {
-        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, true>),
-        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, false>),
-        reinterpret_cast<const void*>(attn::attn_fwd_kernel<true, false, false, true>),
-        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, false, true>),
-        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, false, false>),
-        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, true, true>),
-        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, true, false>),
-        reinterpret_cast<const void*>(attn::attn_fwd_kernel<true, false, true, true>),
-        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, true, true>),
-        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, true, false>)};
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, attn::kModeFull>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, attn::kModeCausal>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, false, attn::kModeGeneral>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<true, false, false, attn::kModeGeneral>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, false, attn::kModeFull>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, false, attn::kModeGeneral>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, true, attn::kModeFull>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, true, attn::kModeCausal>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, false, true, attn::kModeGeneral>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<true, false, true, attn::kModeGeneral>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, true, attn::kModeFull>),
+        reinterpret_cast<const void*>(attn::attn_fwd_kernel<false, true, true, attn::kModeGeneral>)};
     for (const void* fn : fwd_kernels) {
       if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(attn::kSmemBytes)) != cudaSuccess) {
@@ -459,27 +461,28 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
     p.seq = next_seq();
   }
 
-  // Instantiations: <software exp2, split schedule, [B,S,H,D], maskable>; the split schedule is
-  // never used with the software exp2, which is built maskable only.  A launch needs the masking
-  // code only with a ragged last key tile, the causal mask or a zero scale.
+  // Instantiations: <software exp2, split schedule, [B,S,H,D], mode>.  The software exp2 is built
+  // in the general mode only and never with the split schedule, the causal mode never splits.
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const bool soft = (flags & ATTN_FLAG_SOFT_EXP2) != 0;
-  const bool mask = p.causal != 0 || p.kv_valid_last != attn::kBlockN || p.scale_log2 == 0.f ||
-                    Sq % (2 * attn::kBlockM) != 0 || !p.o_align32 || p.test_withhold;
+  const bool general = soft || p.kv_valid_last != attn::kBlockN || p.scale_log2 == 0.f ||
+                       Sq % (2 * attn::kBlockM) != 0 || !p.o_align32 || p.test_withhold;
 #define ATTN_LAUNCH(S, P, L, M) \
   attn::attn_fwd_kernel<S, P, L, M><<<grid, attn::kThreads, attn::kSmemBytes, cs>>>(tm_q, tm_k, tm_v, p)
   if (bshd) {
-    if (soft) ATTN_LAUNCH(true, false, true, true);
-    else if (sp.on && mask) ATTN_LAUNCH(false, true, true, true);
-    else if (sp.on) ATTN_LAUNCH(false, true, true, false);
-    else if (mask) ATTN_LAUNCH(false, false, true, true);
-    else ATTN_LAUNCH(false, false, true, false);
+    if (soft) ATTN_LAUNCH(true, false, true, attn::kModeGeneral);
+    else if (sp.on && general) ATTN_LAUNCH(false, true, true, attn::kModeGeneral);
+    else if (sp.on) ATTN_LAUNCH(false, true, true, attn::kModeFull);
+    else if (general) ATTN_LAUNCH(false, false, true, attn::kModeGeneral);
+    else if (p.causal) ATTN_LAUNCH(false, false, true, attn::kModeCausal);
+    else ATTN_LAUNCH(false, false, true, attn::kModeFull);
   } else {
-    if (soft) ATTN_LAUNCH(true, false, false, true);
-    else if (sp.on && mask) ATTN_LAUNCH(false, true, false, true);
-    else if (sp.on) ATTN_LAUNCH(false, true, false, false);
-    else if (mask) ATTN_LAUNCH(false, false, false, true);
-    else ATTN_LAUNCH(false, false, false, false);
+    if (soft) ATTN_LAUNCH(true, false, false, attn::kModeGeneral);
+    else if (sp.on && general) ATTN_LAUNCH(false, true, false, attn::kModeGeneral);
+    else if (sp.on) ATTN_LAUNCH(false, true, false, attn::kModeFull);
+    else if (general) ATTN_LAUNCH(false, false, false, attn::kModeGeneral);
+    else if (p.causal) ATTN_LAUNCH(false, false, false, attn::kModeCausal);
+    else ATTN_LAUNCH(false, false, false, attn::kModeFull);
   }
 #undef ATTN_LAUNCH
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;

@@ -102,6 +102,18 @@ constexpr uint32_t kColP = 64;   // packed P sits over S columns 64..127 of its 
 // warp-uniform registers.
 constexpr uint32_t kTmemBase = 0;
 
+// Kernel modes (template argument kMode): which cases an instantiation carries code for.
+//   kModeFull:    dense launches with nothing masked or ragged (Sq a multiple of 256, Sk of 128,
+//                 a non-zero scale, a 32-byte-aligned output): every work item has two Q tiles
+//                 over the same KV tiles.
+//   kModeCausal:  the same launches with the causal mask: masking on the diagonal tile only,
+//                 stages of unequal length.
+//   kModeGeneral: everything (ragged lengths, zero scale, one-Q-tile items, 16-byte output
+//                 stores, the failure-path test hook).
+// Code that a launch never runs still costs this kernel (instruction fetch), so each launch
+// takes the leanest mode that covers it.
+constexpr int kModeFull = 0, kModeCausal = 1, kModeGeneral = 2;
+
 // Device status bits (bounded waits that expired, by role).
 constexpr unsigned kStatusTimeoutLoad = 1u << 0;
 constexpr unsigned kStatusTimeoutMma = 1u << 1;
@@ -375,7 +387,7 @@ struct Ctx {
 // ------------------------------------------------------------------ TMA warp
 // kBshd: the layout is a template parameter, so each instantiation's TMA warp holds only its own
 // tensor-map rank (a run-time layout branch in the box loads measured up to 3% slower).
-template <bool kSplit, bool kBshd, bool kMaskable>
+template <bool kSplit, bool kBshd, int kMode>
 __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const CUtensorMap* tm_q,
                                           const CUtensorMap* tm_k, const CUtensorMap* tm_v) {
   SmemCtl* ctl = c.ctl;
@@ -410,7 +422,7 @@ __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const C
     }
   };
   // (the test hook exists in the maskable instantiations only; the host sends its launches there)
-  bool withhold = kMaskable && p.test_withhold != 0 && blockIdx.x == 0;
+  bool withhold = kMode == kModeGeneral && p.test_withhold != 0 && blockIdx.x == 0;
   auto load_kv = [&](const CUtensorMap* tm, int bh, int row) -> bool {
     if (!c.wait(ctl->kv_empty[slot], phase ^ 1u, kStatusTimeoutLoad)) return false;
     if (__builtin_expect(withhold, 0)) {   // the slot is skipped: nothing is loaded into it, nothing to drain
@@ -457,7 +469,7 @@ __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const C
     }
 #endif
     ok = load_q(0, w.bh, row0) && load_kv(tm_k, w.bh, kv0);
-    if (ok && (!kMaskable || w.n[1] > 0)) ok = load_q(1, w.bh, row0 + kBlockM);
+    if (ok && (kMode != kModeGeneral || w.n[1] > 0)) ok = load_q(1, w.bh, row0 + kBlockM);
     if (ok) ok = load_kv(tm_v, w.bh, kv0);
     for (int j = 1; ok && j < ntiles; ++j) {
 #if ATTN_L2_PREFETCH > 0
@@ -505,11 +517,11 @@ __device__ __forceinline__ void issue_pv(const Ctx& c, int vslot, bool overwrite
   }
 }
 
-template <bool kSplit, bool kMaskable>
+template <bool kSplit, int kMode>
 __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
   // The instantiation without masking runs only launches whose work items all have two Q tiles
   // over the same KV tiles (dense, an even number of full Q tiles), so both stages have n tiles.
-  constexpr bool kEq = !kMaskable;
+  constexpr bool kEq = kMode == kModeFull;
   SmemCtl* ctl = c.ctl;
   const bool leader = ptx::elect_one();
   int slot = 0;
@@ -761,15 +773,15 @@ __device__ __forceinline__ bool epilogue_read(const Ctx& c, int q, uint32_t o_pa
 // are computed but not stored).  The row (256 bytes) goes out in 32-byte stores when the output
 // is 32-byte aligned (half the store instructions of 16-byte ones: measured +1.2% at S=4K and
 // +2.8% causal, where item boundaries are frequent), else in 16-byte stores.  LSE = (kept max + log2 l) * ln 2, l the row sum of the fp32 P.
-template <bool kMaskable>
+template <int kMode>
 __device__ __forceinline__ void epilogue_store(const Params& p, int q, const WorkItem& w, int row,
                                                float m, float l, const uint32_t (&pk)[64]) {
   const int grow = (w.qt0 + q) * kBlockM + row;
-  if (kMaskable && grow >= p.sq) return;   // (no ragged Q rows in the other instantiations)
+  if (kMode == kModeGeneral && grow >= p.sq) return;   // (no ragged Q rows in the other modes)
   const int b = w.bh / p.heads, h = w.bh - b * p.heads;
   uint8_t* out = static_cast<uint8_t*>(p.o) +
                  (b * p.o_batch_stride + h * p.o_head_stride + grow * p.o_row_stride) * 2;
-  if (!kMaskable || __builtin_expect(p.o_align32, 1)) {   // 32-byte stores where allowed
+  if (kMode != kModeGeneral || __builtin_expect(p.o_align32, 1)) {   // 32-byte stores where allowed
 #pragma unroll
     for (int i = 0; i < 8; ++i) ptx::st_global_v8(out + 32 * i, pk + 8 * i);
   } else {
@@ -911,7 +923,7 @@ __device__ __noinline__ bool epilogue_split(const Ctx& c, const SplitOut p, int 
   return true;
 }
 
-template <bool kSoftExp2, bool kSplit, bool kMaskable>
+template <bool kSoftExp2, bool kSplit, int kMode>
 __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int q) {
   SmemCtl* ctl = c.ctl;
   const uint32_t row_base = 32u * (c.warp & 3u);
@@ -919,7 +931,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
   const uint32_t taddr_s = c.tmem + (row_base << 16) + col_s(q);
   // A zero scale makes every kept score 0 (mask_scores on every tile) and uses multiplier 1, so
   // masked columns still give -inf * 1 = -inf rather than -inf * 0 = NaN.
-  const bool zero_scale = kMaskable && p.scale_log2 == 0.f;
+  const bool zero_scale = kMode == kModeGeneral && p.scale_log2 == 0.f;
   const float scale_log2 = zero_scale ? 1.f : p.scale_log2;
   const uint32_t keep = zero_scale ? 0u : 0xffffffffu;
   uint32_t tphase = 0;
@@ -933,7 +945,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
     if (!seg_of<kSplit>(r, p, ctl->sk_range, sg)) break;
     const WorkItem& w = sg.w;
     const int ntiles = w.n[q];
-    if (kMaskable && ntiles == 0) continue;
+    if (kMode == kModeGeneral && ntiles == 0) continue;
     const int qtile = w.qt0 + q;
     // The previous item's epilogue, before this item's first P: its O columns are then free
     // when that P is published (the first P*V of an item overwrites O), and the read overlaps
@@ -944,7 +956,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
       } else {
         uint32_t pk[64];
         if (!epilogue_read(c, q, o_parity, 1.0f / lr_prev, pk)) return;
-        epilogue_store<kMaskable>(p, q, sp.w, row, m_prev, l_prev, pk);
+        epilogue_store<kMode>(p, q, sp.w, row, m_prev, l_prev, pk);
       }
       o_parity ^= 1u;
     }
@@ -963,13 +975,16 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
       // tile.  They must not enter the max and get P = 0 below.  The test is warp-uniform.
       const int jg = sg.j0 + j;   // KV tile index within the head
       const bool diag = p.causal != 0 && jg == qtile;
-      // kMaskable: the launch may have masked columns (a ragged last key tile, the causal diagonal
-      // or a zero scale).  The instantiation for launches without any has no masking code: its
+      // Tiles with masked columns: the causal diagonal (kModeCausal), also a ragged last key tile
+      // and every tile at zero scale (kModeGeneral); kModeFull has no masking code, whose
       // presence, never taken, cost the dense forward ~2% (same-box A/B, bitwise the same).
       const bool partial =
-          kMaskable && (zero_scale || diag || (jg == p.kv_tiles - 1 && p.kv_valid_last < kBlockN));
+          kMode == kModeCausal ? diag
+          : kMode == kModeGeneral
+              ? (zero_scale || diag || (jg == p.kv_tiles - 1 && p.kv_valid_last < kBlockN))
+              : false;
       int valid = kBlockN;
-      if (jg == p.kv_tiles - 1) valid = p.kv_valid_last;
+      if (kMode == kModeGeneral && jg == p.kv_tiles - 1) valid = p.kv_valid_last;
       if (diag) valid = min(valid, row + 1);
       if (partial) mask_scores(sr, valid, keep);
 
@@ -1009,7 +1024,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
     } else {
       uint32_t pk[64];
       if (!epilogue_read(c, q, o_parity, 1.0f / lr_prev, pk)) return;
-      epilogue_store<kMaskable>(p, q, sp.w, row, m_prev, l_prev, pk);
+      epilogue_store<kMode>(p, q, sp.w, row, m_prev, l_prev, pk);
     }
   }
 }
@@ -1017,7 +1032,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
 // ------------------------------------------------------------------ correction warpgroup
 // Per KV tile and stage: if any row of the warp rebased its max, O_q *= alpha in TMEM; then O_q
 // is safe for the next P*V (p_full, together with the softmax's P).
-template <bool kSplit, bool kMaskable>
+template <bool kSplit, int kMode>
 __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
   SmemCtl* ctl = c.ctl;
   const uint32_t row_base = 32u * (c.warp & 3u);
@@ -1032,7 +1047,7 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
     for (int j = 0; j < ntiles; ++j) {
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        if (kMaskable && j >= w.n[q]) continue;
+        if (kMode != kModeFull && j >= w.n[q]) continue;
         if (!c.wait(ctl->stats_full[q], tphase[q], kStatusTimeoutCorrection)) return;
         // alpha is 1 on an item's first tile, so the previous item's O, which its softmax
         // warpgroup may still be reading, is not touched here.
@@ -1060,7 +1075,7 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
 }
 
 // ------------------------------------------------------------------ kernel
-template <bool kSoftExp2, bool kSplit, bool kBshd, bool kMaskable>
+template <bool kSoftExp2, bool kSplit, bool kBshd, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -1113,14 +1128,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (threadIdx.x == 0) atomicOr(&g_attn_status, kStatusTmemBase);
   } else if (c.warp < kCorrWarp0) {
     ptx::setmaxnreg_inc<kRegSoftmax>();
-    softmax_role<kSoftExp2, kSplit, kMaskable>(c, p, static_cast<int>(c.warp >> 2));
+    softmax_role<kSoftExp2, kSplit, kMode>(c, p, static_cast<int>(c.warp >> 2));
   } else if (c.warp < kLoadWarp) {
     ptx::setmaxnreg_dec<kRegCorr>();
-    correction_role<kSplit, kMaskable>(c, p);
+    correction_role<kSplit, kMode>(c, p);
   } else {
     ptx::setmaxnreg_dec<kRegMisc>();
-    if (c.warp == kLoadWarp) load_role<kSplit, kBshd, kMaskable>(c, p, &tm_q, &tm_k, &tm_v);
-    else if (c.warp == kMmaWarp) mma_role<kSplit, kMaskable>(c, p);
+    if (c.warp == kLoadWarp) load_role<kSplit, kBshd, kMode>(c, p, &tm_q, &tm_k, &tm_v);
+    else if (c.warp == kMmaWarp) mma_role<kSplit, kMode>(c, p);
   }
 
   ptx::tc_fence_before();
