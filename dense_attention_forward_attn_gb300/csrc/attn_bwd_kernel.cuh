@@ -202,9 +202,10 @@ __device__ __forceinline__ void prefetch_tile(const CUtensorMap* tm, int row, in
   }
 }
 
-// Byte offset of row `row` of head bh in a BF16 [B,H,S,128] or [B,S,H,128] tensor.
+// Byte offset of row `row` of head bh in a BF16 [B,H,S,128] or (kBshd) [B,S,H,128] tensor.
+template <bool kBshd>
 __device__ __forceinline__ size_t row_offset(const Params& p, int bh, int row, int seq) {
-  if (p.bshd) {
+  if (kBshd) {
     const int b = bh / p.heads, h = bh - b * p.heads;
     return ((static_cast<size_t>(b) * seq + row) * p.heads + h) * (kHeadDim * 2);
   }
@@ -425,7 +426,7 @@ __device__ __forceinline__ void dq_p(const uint32_t (&sr)[4][32], float2 sl2, fl
 
 // kMask: the launch may have masked keys (a ragged last K/V tile or the causal mask); the
 // instantiation for launches without any has no masking code.
-template <bool kMask>
+template <bool kMask, bool kBshd>
 __global__ void __launch_bounds__(kDqThreads, 1)
 attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -435,7 +436,8 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     if (threadIdx.x == 0) atomicOr(&g_attn_status, kStatusSmemAlign);
     return;
   }
-  const Layout L = setup(smem_raw, kCtlOffsetDq, p);
+  Layout L = setup(smem_raw, kCtlOffsetDq, p);
+  L.heads4d = kBshd ? p.heads : 0;   // the layout is known at compile time: one tensor-map rank
   SmemCtl* ctl = L.ctl;
   const uint32_t warp = threadIdx.x >> 5;
   Sync s{ctl, threadIdx.x & 31u};
@@ -590,7 +592,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
     if (ok && n[t] > 0 && s.wait(ctl->acc_full, 0, kStatusTimeoutSoftmax)) {
       ptx::tc_fence_after();
-      uint8_t* out = static_cast<uint8_t*>(p.out0) + row_offset(p, bh, qrow, p.sq);
+      uint8_t* out = static_cast<uint8_t*>(p.out0) + row_offset<kBshd>(p, bh, qrow, p.sq);
       const uint32_t acc_col = kTmemBase + (row_base << 16) + kColDQ + 128u * t;
 #pragma unroll 2
       for (int c = 0; c < 8; ++c) {
@@ -656,14 +658,15 @@ __device__ __forceinline__ void dkdv_p(const uint32_t (&xr)[2][32], const float*
 }
 
 // kMask: the launch uses the causal mask (the only per-element masking this kernel does).
-template <bool kMask>
+template <bool kMask, bool kBshd>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                      const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  const Layout L = setup(smem_raw, kCtlOffsetDkdv, p);
+  Layout L = setup(smem_raw, kCtlOffsetDkdv, p);
+  L.heads4d = kBshd ? p.heads : 0;   // the layout is known at compile time: one tensor-map rank
   SmemCtl* ctl = L.ctl;
   const uint32_t warp = threadIdx.x >> 5;
   Sync s{ctl, threadIdx.x & 31u};
@@ -847,7 +850,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       }
     }
     const bool row_ok = krow < p.sk;
-    const size_t gk = row_offset(p, bh, krow, p.sk);
+    const size_t gk = row_offset<kBshd>(p, bh, krow, p.sk);
     if (nq == 0) {
       // keys no query attends (causal, Sk > Sq): zero gradients (dK by warpgroup 0, dV by 1)
       if (row_ok) zero_row(static_cast<uint8_t*>(g == 0 ? p.out0 : p.out1) + gk);

@@ -86,11 +86,16 @@ int device_info(int dev, DeviceInfo* out) {
     d.attr_set = true;
   }
   if (!d.bwd_attr_set) {
-    const void* dq_kernels[] = {reinterpret_cast<const void*>(attn::bwd::attn_bwd_dq_kernel<true>),
-                                reinterpret_cast<const void*>(attn::bwd::attn_bwd_dq_kernel<false>)};
+    const void* dq_kernels[] = {
+        reinterpret_cast<const void*>(attn::bwd::attn_bwd_dq_kernel<true, false>),
+        reinterpret_cast<const void*>(attn::bwd::attn_bwd_dq_kernel<false, false>),
+        reinterpret_cast<const void*>(attn::bwd::attn_bwd_dq_kernel<true, true>),
+        reinterpret_cast<const void*>(attn::bwd::attn_bwd_dq_kernel<false, true>)};
     const void* dkdv_kernels[] = {
-        reinterpret_cast<const void*>(attn::bwd::attn_bwd_dkdv_kernel<true>),
-        reinterpret_cast<const void*>(attn::bwd::attn_bwd_dkdv_kernel<false>)};
+        reinterpret_cast<const void*>(attn::bwd::attn_bwd_dkdv_kernel<true, false>),
+        reinterpret_cast<const void*>(attn::bwd::attn_bwd_dkdv_kernel<false, false>),
+        reinterpret_cast<const void*>(attn::bwd::attn_bwd_dkdv_kernel<true, true>),
+        reinterpret_cast<const void*>(attn::bwd::attn_bwd_dkdv_kernel<false, true>)};
     for (const void* fn : dq_kernels) {
       if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(attn::bwd::kSmemBytesDq)) != cudaSuccess) {
@@ -773,26 +778,31 @@ extern "C" int attn_bwd(const void* q, const void* k, const void* v, const void*
   p.out0 = dk;
   p.out1 = dv;
   // The masking code is compiled only into the instantiations for launches that need it (the
-  // causal mask; for the dQ kernel also a ragged last K/V tile).
+  // causal mask; for the dQ kernel also a ragged last K/V tile), the layout into each one's own.
   const bool mask_dq = p.causal != 0 || p.kv_valid_last != attn::kBlockN;
-  if (p.causal)
-    attn::bwd::attn_bwd_dkdv_kernel<true><<<static_cast<unsigned>(bh * p.kv_tiles), attn::bwd::kThreads,
-                                            attn::bwd::kSmemBytesDkdv, st>>>(tm_q, tm_k, tm_v, tm_do,
-                                                                              tm_dk, tm_dv, p);
-  else
-    attn::bwd::attn_bwd_dkdv_kernel<false><<<static_cast<unsigned>(bh * p.kv_tiles), attn::bwd::kThreads,
-                                             attn::bwd::kSmemBytesDkdv, st>>>(tm_q, tm_k, tm_v, tm_do,
-                                                                               tm_dk, tm_dv, p);
+  const unsigned dkdv_grid = static_cast<unsigned>(bh * p.kv_tiles);
+  const unsigned dq_grid = static_cast<unsigned>(bh * ((p.q_tiles + 1) / 2));
+#define ATTN_DKDV(M, L)                                                                      \
+  attn::bwd::attn_bwd_dkdv_kernel<M, L><<<dkdv_grid, attn::bwd::kThreads,                   \
+                                          attn::bwd::kSmemBytesDkdv, st>>>(tm_q, tm_k, tm_v, \
+                                                                           tm_do, tm_dk, tm_dv, p)
+#define ATTN_DQ(M, L)                                                                           \
+  attn::bwd::attn_bwd_dq_kernel<M, L><<<dq_grid, attn::bwd::kDqThreads, attn::bwd::kSmemBytesDq, \
+                                        F.side>>>(tm_q, tm_k, tm_v, tm_do, p)
+  if (p.causal) {
+    if (bshd) ATTN_DKDV(true, true); else ATTN_DKDV(true, false);
+  } else {
+    if (bshd) ATTN_DKDV(false, true); else ATTN_DKDV(false, false);
+  }
   p.out0 = dq;
   p.out1 = nullptr;
-  if (mask_dq)
-    attn::bwd::attn_bwd_dq_kernel<true><<<static_cast<unsigned>(bh * ((p.q_tiles + 1) / 2)),
-                                          attn::bwd::kDqThreads, attn::bwd::kSmemBytesDq, F.side>>>(
-        tm_q, tm_k, tm_v, tm_do, p);
-  else
-    attn::bwd::attn_bwd_dq_kernel<false><<<static_cast<unsigned>(bh * ((p.q_tiles + 1) / 2)),
-                                           attn::bwd::kDqThreads, attn::bwd::kSmemBytesDq, F.side>>>(
-        tm_q, tm_k, tm_v, tm_do, p);
+  if (mask_dq) {
+    if (bshd) ATTN_DQ(true, true); else ATTN_DQ(true, false);
+  } else {
+    if (bshd) ATTN_DQ(false, true); else ATTN_DQ(false, false);
+  }
+#undef ATTN_DKDV
+#undef ATTN_DQ
   const bool launched = cudaGetLastError() == cudaSuccess;
   // Join even after a failed launch, so the caller's stream never runs ahead of a dQ in flight.
   if (cudaEventRecord(F.join, F.side) != cudaSuccess || cudaStreamWaitEvent(st, F.join, 0) != cudaSuccess) {
