@@ -421,7 +421,7 @@ __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const C
       ptx::tma_prefetch_3d(tm, 64, row, bh);
     }
   };
-  // (the test hook exists in the maskable instantiations only; the host sends its launches there)
+  // (the test hook exists in the general mode only; the host sends its launches there)
   bool withhold = kMode == kModeGeneral && p.test_withhold != 0 && blockIdx.x == 0;
   auto load_kv = [&](const CUtensorMap* tm, int bh, int row) -> bool {
     if (!c.wait(ctl->kv_empty[slot], phase ^ 1u, kStatusTimeoutLoad)) return false;
