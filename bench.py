@@ -214,9 +214,16 @@ def oracle_sample_tflops(shapes, seconds: float, seed: int = 0):
     return total_flops / total_t / 1e12, threads, ", ".join(rows_done), total_t
 
 
-def bench_config(workload, shapes, reps, ws):
+def bench_config(workload, shapes, reps, ws, causal=False, layout="bhsd"):
     """The `config` object of the JSON line, the same for both arms."""
-    return {"workload": workload, "shapes": [w.describe() for w in shapes],
+    described = []
+    for w in shapes:
+        d = w.describe()
+        d["causal"] = bool(causal)
+        if layout == "bshd":
+            d["layout"] = "BSHD contiguous"
+        described.append(d)
+    return {"workload": workload, "shapes": described,
             "problems_per_shape_per_step": reps,
             "l2": "inputs larger than L2 (Q+K+V = 192 MiB per problem); consecutive launches read "
                   "different problems' inputs",
@@ -444,7 +451,8 @@ def run_ours(args):
         "timed_region_s": round(total_ms / 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": bench_config(workload, [w for w, *_ in shapes], reps, ws),
+        "config": bench_config(workload, [w for w, *_ in shapes], reps, ws, causal=causal,
+                               layout=layout),
         "detail": {"per_shape": per_cfg, "frac_of_peak": round(value / peak, 4),
                    "frac_of_burst_peak": round(value / peak_burst, 4),
                    "device_status": status,
