@@ -408,6 +408,19 @@ __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const C
       ptx::tma_load_3d(dst, tm, fb, col, row, bh);
     }
   };
+  // Causal mode: the heaviest-first order keeps every head's K/V in use for the whole launch,
+  // more than L2 holds at S=4K (B=4, H=16: 128 MiB); Q tiles, read once, are marked first to
+  // evict so they do not push K/V lines out (+1.0% at causal S=4K, +0.6% at S=16K).
+  auto load_q_box = [&](uint32_t dst, uint32_t fb, int col, int row, int bh) {
+    if (kMode != kModeCausal) {
+      load_box(dst, tm_q, fb, col, row, bh);
+    } else if (kBshd) {
+      const int b = bh / p.heads, h = bh - b * p.heads;
+      ptx::tma_load_4d_hint(dst, tm_q, fb, col, h, row, b, ptx::l2_policy_evict_first());
+    } else {
+      ptx::tma_load_3d_hint(dst, tm_q, fb, col, row, bh, ptx::l2_policy_evict_first());
+    }
+  };
   // L2 prefetch of a K or V tile ATTN_L2_PREFETCH tiles ahead of its load: the first CTA to
   // read a tile of a head otherwise waits for DRAM, and so do the CTAs reading it with it.
   auto prefetch = [&](const CUtensorMap* tm, int bh, int row) {
@@ -447,8 +460,8 @@ __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const C
     if (c.lane == 0) {
       const uint32_t fb = c.bar(ctl->q_full[q]);
       ptx::mbar_arrive_expect_tx(fb, kTileBytes);
-      load_box(c.sq(q), tm_q, fb, 0, row, bh);
-      load_box(c.sq(q) + kSlabBytes, tm_q, fb, 64, row, bh);
+      load_q_box(c.sq(q), fb, 0, row, bh);
+      load_q_box(c.sq(q) + kSlabBytes, fb, 64, row, bh);
     }
     __syncwarp();
     ++q_cnt[q];
@@ -781,7 +794,11 @@ __device__ __forceinline__ void epilogue_store(const Params& p, int q, const Wor
   const int b = w.bh / p.heads, h = w.bh - b * p.heads;
   uint8_t* out = static_cast<uint8_t*>(p.o) +
                  (b * p.o_batch_stride + h * p.o_head_stride + grow * p.o_row_stride) * 2;
-  if (kMode != kModeGeneral || __builtin_expect(p.o_align32, 1)) {   // 32-byte stores where allowed
+  if (kMode == kModeCausal) {   // written once: first to evict from L2 (as the Q tiles)
+    const uint64_t pol = ptx::l2_policy_evict_first();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ptx::st_global_v8_hint(out + 32 * i, pk + 8 * i, pol);
+  } else if (kMode != kModeGeneral || __builtin_expect(p.o_align32, 1)) {   // 32-byte stores where allowed
 #pragma unroll
     for (int i = 0; i < 8; ++i) ptx::st_global_v8(out + 32 * i, pk + 8 * i);
   } else {
