@@ -611,11 +611,14 @@ __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
         return qk(q, next_kslot, true, nw.n[q] == 1, q == 1 || nw.n[1] == 0);
       };
       bool next0_done = false;
-      if constexpr (kMode == kModeCausal) {
-        // Causal pairs: n1 = n0 + d, d in {0, 1}.  The tiles both stages share run a loop
+      if constexpr (kMode == kModeCausal || (kSplit && kMode == kModeFull)) {
+        // Causal pairs: n1 = n0 + d, d in {0, 1} (d = 0 in the split instantiation, whose
+        // segments give both stages the same KV range).  The tiles both stages share run a loop
         // without per-stage tests; stage 0's last tile and stage 1's extra one follow (the same
         // MMAs and commits in the same order as the loop below; the MMA warp's instructions per
-        // tile bound this pipeline: +1.4% at causal S=4K, +2.4% at S=16K).
+        // tile bound this pipeline: +1.4% at causal S=4K, +2.4% at S=16K, +2.6% for the split
+        // schedule at S=16K; the whole-item full-tile instantiation measured -0.6 to -0.9% with
+        // it and keeps the loop below).
         const int d = n1 - n0;
         for (int j = 0; ok && j < n0 - 1; ++j) {
           const int vslot = slot;
