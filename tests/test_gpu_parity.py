@@ -383,9 +383,9 @@ def test_bshd_layout(shape, causal):
     assert torch.equal(o2, o.transpose(1, 2).contiguous()) and torch.equal(lse2, lse)
 
 
-@pytest.mark.parametrize("name", ["S=4K", "S=16K"])
+@pytest.mark.parametrize("name", ["S=4K", "S=8K", "S=16K"])
 def test_bshd_full_size_sampled_rows(name):
-    """The benchmark's [B,S,H,D] launches (S=4K whole items, S=16K the split schedule): bitwise
+    """The benchmark's [B,S,H,D] launches (S=4K whole items, S=8K and S=16K the split schedule): bitwise
     equal to [B,H,S,D] on the same values (whose every element test_full_size_workload_every_element
     compares with the oracle), and sampled rows against the oracle directly."""
     w = wl.ALL[name]
