@@ -105,7 +105,8 @@ constexpr uint32_t kTmemBase = 0;
 // Kernel modes (template argument kMode): which cases an instantiation carries code for.
 //   kModeFull:    dense launches with nothing masked or ragged (Sq a multiple of 256, Sk of 128,
 //                 a non-zero scale, a 32-byte-aligned output): every work item has two Q tiles
-//                 over the same KV tiles.
+//                 over the same KV tiles.  Built with the split schedule only (a launch without
+//                 split items runs it with an empty split part).
 //   kModeCausal:  the same launches with the causal mask: masking on the diagonal tile only,
 //                 stages of unequal length.
 //   kModeGeneral: everything (ragged lengths, zero scale, one-Q-tile items, 16-byte output
@@ -532,9 +533,6 @@ __device__ __forceinline__ void issue_pv(const Ctx& c, int vslot, bool overwrite
 
 template <bool kSplit, int kMode>
 __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
-  // The instantiation without masking runs only launches whose work items all have two Q tiles
-  // over the same KV tiles (dense, an even number of full Q tiles), so both stages have n tiles.
-  constexpr bool kEq = kMode == kModeFull;
   SmemCtl* ctl = c.ctl;
   const bool leader = ptx::elect_one();
   int slot = 0;
@@ -599,7 +597,10 @@ __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
     if (ok && w.n[1] > 0) ok = qk(1, kslot, true, w.n[1] == 1, true);
     while (ok) {
       const int ntiles = w.n[1] > 0 ? w.n[1] : w.n[0];
-      const int n0 = kEq ? ntiles : w.n[0], n1 = kEq ? ntiles : w.n[1];
+      // The full-tile mode's items all have two Q tiles over the same KV tiles (dense, an even
+      // number of full Q tiles; a split segment gives both the same KV range): n0 = n1.
+      const int n0 = kMode == kModeFull ? ntiles : w.n[0];
+      const int n1 = kMode == kModeFull ? ntiles : w.n[1];
       Seg nsg;
       const bool has_next = seg_of<kSplit>(r + 1, p, ctl->sk_range, nsg);
       const WorkItem nw = has_next ? nsg.w : w;
@@ -611,14 +612,12 @@ __device__ __forceinline__ void mma_role(const Ctx& c, const Params& p) {
         return qk(q, next_kslot, true, nw.n[q] == 1, q == 1 || nw.n[1] == 0);
       };
       bool next0_done = false;
-      if constexpr (kMode == kModeCausal || (kSplit && kMode == kModeFull)) {
-        // Causal pairs: n1 = n0 + d, d in {0, 1} (d = 0 in the split instantiation, whose
-        // segments give both stages the same KV range).  The tiles both stages share run a loop
-        // without per-stage tests; stage 0's last tile and stage 1's extra one follow (the same
-        // MMAs and commits in the same order as the loop below; the MMA warp's instructions per
-        // tile bound this pipeline: +1.4% at causal S=4K, +2.4% at S=16K, +2.6% for the split
-        // schedule at S=16K; the whole-item full-tile instantiation measured -0.6 to -0.9% with
-        // it and keeps the loop below).
+      if constexpr (kMode != kModeGeneral) {
+        // n1 = n0 + d, d in {0, 1}: d = 1 for most causal pairs, 0 in the full-tile mode.  The
+        // tiles both stages share run a loop without per-stage tests; stage 0's last tile and
+        // stage 1's extra one follow (the same MMAs and commits in the same order as the general
+        // loop below; the MMA warp's instructions per tile bound this pipeline: +1.4% at causal
+        // S=4K, +2.4% at causal S=16K, +2.6% for the split schedule at S=16K, bitwise the same).
         const int d = n1 - n0;
         for (int j = 0; ok && j < n0 - 1; ++j) {
           const int vslot = slot;
