@@ -133,7 +133,10 @@ struct alignas(8) SmemCtl {
   uint64_t p_full[2];      // softmax (P in TMEM) + correction (O rescaled or untouched) -> MMA
   uint64_t stats_full[2];  // softmax -> correction: per-row rescale factor published
   uint64_t o_full[2];      // MMA -> epilogue: last P*V of the item done (O final in TMEM)
-  uint64_t fin_full[2];    // softmax -> correction: an item's final row statistics
+  uint64_t fin_full[2][2]; // softmax -> correction: an item's final row statistics, per fin
+                           // slot (a stage's softmax can finish two short items before the
+                           // correction reads the first: one barrier per slot keeps each
+                           // barrier at most one phase ahead of its waiter)
   uint64_t drain;
   uint32_t tmem_base;
   volatile int abort_flag;
@@ -1021,7 +1024,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
   bool have_prev = false;    // an item whose epilogue is still to do
   Seg sp;
   float m_prev = 0.f, l_prev = 1.f, lr_prev = 1.f;
-  uint32_t fin_par = 0;   // item parity of ctl->fin (causal mode)
+  uint32_t fin_par = 0;   // ctl->fin slot of the next item the correction warpgroup finishes
 
   for (int r = 0;; ++r) {
     Seg sg;
@@ -1101,7 +1104,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
       // warpgroup goes on with the next item (a split item's part is finished here, below).
       ctl->fin[q][fin_par][row] =
           make_float2(1.0f / (l + dl), (m_kept + log2f(l)) * 0.69314718055994530942f);
-      c.arrive(ctl->fin_full[q]);
+      c.arrive(ctl->fin_full[q][fin_par]);
       fin_par ^= 1u;
     }
     have_prev = true;
@@ -1137,7 +1140,8 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
   // epilogue here from the softmax warpgroups measured +1.2% at S=4K, +1.0% at S=8K/16K (split
   // schedule), +2.8% / +2.4% at causal S=4K / 16K (same box, bitwise the same).
   uint32_t opar[2] = {0, 0};   // o_full phase of the previous item (every item)
-  uint32_t fpar[2] = {0, 0};   // fin_full phase and ctl->fin slot (items finished here)
+  uint32_t fcnt[2] = {0, 0};   // items finished here per stage: ctl->fin slot fcnt & 1,
+                               // that slot's fin_full phase (fcnt >> 1) & 1
   Seg prev;
   bool have_prev = false;
   auto epilogue = [&](int q, const Seg& sgp) -> bool {
@@ -1146,9 +1150,10 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
     opar[q] ^= 1u;
     if (kSplit && sgp.slot >= 0) return true;   // a split item's part: the softmax finishes it
     const WorkItem& w = sgp.w;
-    if (!c.wait(ctl->fin_full[q], fpar[q], kStatusTimeoutCorrection)) return false;
+    const uint32_t slot = fcnt[q] & 1u;
+    if (!c.wait(ctl->fin_full[q][slot], (fcnt[q] >> 1) & 1u, kStatusTimeoutCorrection)) return false;
     ptx::tc_fence_after();
-    const float2 f = ctl->fin[q][fpar[q]][row];
+    const float2 f = ctl->fin[q][slot][row];
     const uint32_t taddr_o = c.tmem + (row_base << 16) + col_o(q);
     const int grow = (w.qt0 + q) * kBlockM + row;
     const int b = w.bh / p.heads, h = w.bh - b * p.heads;
@@ -1169,7 +1174,7 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
     }
     if (p.lse != nullptr) p.lse[static_cast<size_t>(w.bh) * p.sq + grow] = f.y;
     ptx::tc_fence_before();
-    fpar[q] ^= 1u;
+    ++fcnt[q];
     return true;
   };
 
@@ -1239,7 +1244,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       ptx::mbar_init(c.bar(ctl->p_full[q]), 2 * kArrivePerWG);   // softmax + correction WGs
       ptx::mbar_init(c.bar(ctl->stats_full[q]), kArrivePerWG);
       ptx::mbar_init(c.bar(ctl->o_full[q]), 1);
-      ptx::mbar_init(c.bar(ctl->fin_full[q]), kArrivePerWG);
+      ptx::mbar_init(c.bar(ctl->fin_full[q][0]), kArrivePerWG);
+      ptx::mbar_init(c.bar(ctl->fin_full[q][1]), kArrivePerWG);
     }
     for (int s = 0; s < kKvStages; ++s) {
       ptx::mbar_init(c.bar(ctl->kv_full[s]), 1);
