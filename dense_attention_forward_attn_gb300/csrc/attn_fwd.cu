@@ -182,8 +182,9 @@ int check_shape(int B, int H, int Sq, int Sk, int D) {
 // shortens the longest CTA by at least kSplitMinGainTiles KV tiles.  Every extra segment of a CTA
 // costs ~2 us of pipeline fill and drain, the combining epilogue ~3 us, and with all CTAs given
 // equal work the slowest SM sets the end.  Measured on GB300 (split against whole items, same box,
-// with the split instantiation's lean MMA loop): S=4K at 16 heads (8 tiles shorter) 0.0%, S=8K
-// at 16 heads (16 tiles) +2.9%, S=16K at 16 heads (33 tiles) +3.2%, S=12K at 24 heads (40) +2.8%.
+// with the split instantiation's lean MMA loop): S=8K at 16 heads (16 tiles shorter) +2.9%, S=16K
+// at 16 heads (33 tiles) +3.2%, S=12K at 24 heads (40) +2.8%; S=4K at 16 heads (8 tiles) 0.0%,
+// and +0.9% once whole items' epilogue moved to the correction warpgroup ([B,S,H,D]: +1.7%).
 // Dense, non-causal, exp2 on MUFU only.
 struct SplitPlan {
   bool on = false;
@@ -200,7 +201,7 @@ SplitPlan split_plan(int64_t items, int grid, int kv_tiles, int flags) {
   const int64_t units = sk_items * kv_tiles;
   if (units * grid > INT32_MAX) return sp;   // the kernel's unit arithmetic is 32-bit
   const int64_t longest = (units + grid - 1) / grid;
-  constexpr int64_t kSplitMinGainTiles = 12;
+  constexpr int64_t kSplitMinGainTiles = 8;
   if (2 * static_cast<int64_t>(kv_tiles) - longest < kSplitMinGainTiles) return sp;
   sp.on = true;
   sp.sk_item0 = static_cast<int>(sk_item0);

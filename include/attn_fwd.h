@@ -138,10 +138,10 @@ int attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse
  *   workspace_bytes  its size
  *
  * The split schedule is used for dense, non-causal calls without
- * ATTN_FLAG_SOFT_EXP2 where it shortens the longest CTA by at least 12
+ * ATTN_FLAG_SOFT_EXP2 where it shortens the longest CTA by at least 8
  * KV-tile iterations (each extra segment and the combine cost a few; on a
- * 152-SM GPU: S=8K and S=16K at 16 heads and S=12K at 24 heads split, S=4K at
- * 16 heads does not); otherwise this is attn_fwd_ex and the workspace is not
+ * 152-SM GPU: S=4K, S=8K and S=16K at 16 heads and S=12K at 24 heads split,
+ * S=2K at 16 heads does not); otherwise this is attn_fwd_ex and the workspace is not
  * touched.  A workspace must not be used by two calls that can run at the same time
  * (different streams): they would overwrite each other's partial results.
  * Errors as attn_fwd_ex, plus ATTN_ERR_INVALID_ARG for a missing, short,

@@ -385,7 +385,7 @@ def test_bshd_layout(shape, causal):
 
 @pytest.mark.parametrize("name", ["S=4K", "S=8K", "S=16K"])
 def test_bshd_full_size_sampled_rows(name):
-    """The benchmark's [B,S,H,D] launches (S=4K whole items, S=8K and S=16K the split schedule): bitwise
+    """The benchmark's [B,S,H,D] launches (the split schedule at each shape): bitwise
     equal to [B,H,S,D] on the same values (whose every element test_full_size_workload_every_element
     compares with the oracle), and sampled rows against the oracle directly."""
     w = wl.ALL[name]

@@ -266,9 +266,9 @@ def test_split_schedule_covers_every_unit_once_and_pairs_the_parts(lib, items, g
 
 
 def test_split_schedule_is_used_where_it_pays(lib):
-    # S=8K and S=16K at 16 heads and S=12K at 24 heads split (the longest CTA gets >= 12 KV
-    # tiles shorter: 16, 33 and 40); S=4K at 16 heads (8 tiles), whole rounds, short KV ranges
-    # and causal calls do not
+    # S=4K, S=8K and S=16K at 16 heads and S=12K at 24 heads split (the longest CTA gets >= 8
+    # KV tiles shorter: 8, 16, 33 and 40); S=2K at 16 heads (4 tiles), whole rounds, short KV
+    # ranges and causal calls do not
     def split(items, grid, n, causal=False):
         for c in range(grid):
             r = 0
@@ -278,15 +278,16 @@ def test_split_schedule_is_used_where_it_pays(lib):
                 r += 1
         return False
 
-    assert split(1024, 152, 128) and split(1024, 152, 64) and not split(1024, 152, 32)
+    assert split(1024, 152, 128) and split(1024, 152, 64) and split(1024, 152, 32)
+    assert not split(1024, 152, 16)
     assert split(1152, 152, 96)   # S=12K at 24 heads: 7.58 rounds
     assert not split(1216, 152, 96) and not split(400, 152, 1) and not split(100, 152, 8)
     assert not split(1024, 152, 128, causal=True)
     # 1136 items: 7.47 rounds, but 128 KV tiles per item gain 68 tiles from an even division
     assert split(1136, 152, 128)
-    # 1144 items: 7.53 rounds of 32 tiles gain 15; 1100 items of 12 tiles gain 9, of 16 tiles 12
+    # 1144 items: 7.53 rounds of 32 tiles gain 15; 1100 items of 8 tiles gain 6, of 12 tiles 9
     assert split(1144, 152, 32)
-    assert not split(1100, 152, 12) and split(1100, 152, 16)
+    assert not split(1100, 152, 8) and split(1100, 152, 12)
 
 
 def test_split_entry_point_checks_before_any_cuda_call(lib):
