@@ -850,23 +850,19 @@ __device__ __forceinline__ bool epilogue_read(const Ctx& c, int q, uint32_t o_pa
   return true;
 }
 
-// O row and LSE of this thread's query row of stage q of item w (rows past a ragged end of Q
-// are computed but not stored).  The row (256 bytes) goes out in 32-byte stores when the output
-// is 32-byte aligned (half the store instructions of 16-byte ones: measured +1.2% at S=4K and
-// +2.8% causal, where item boundaries are frequent), else in 16-byte stores.  LSE = (kept max + log2 l) * ln 2, l the row sum of the fp32 P.
-template <int kMode>
+// General mode: O row and LSE of this thread's query row of stage q of item w (rows past a ragged
+// end of Q are computed but not stored).  The row (256 bytes) goes out in 32-byte stores when the
+// output is 32-byte aligned (half the store instructions of 16-byte ones: measured +1.2% at S=4K
+// and +2.8% causal when this epilogue served every mode), else in 16-byte stores.
+// LSE = (kept max + log2 l) * ln 2, l the row sum of the fp32 P.
 __device__ __forceinline__ void epilogue_store(const Params& p, int q, const WorkItem& w, int row,
                                                float m, float l, const uint32_t (&pk)[64]) {
   const int grow = (w.qt0 + q) * kBlockM + row;
-  if (kMode == kModeGeneral && grow >= p.sq) return;   // (no ragged Q rows in the other modes)
+  if (grow >= p.sq) return;
   const int b = w.bh / p.heads, h = w.bh - b * p.heads;
   uint8_t* out = static_cast<uint8_t*>(p.o) +
                  (b * p.o_batch_stride + h * p.o_head_stride + grow * p.o_row_stride) * 2;
-  if (kMode == kModeCausal) {   // written once: first to evict from L2 (as the Q tiles)
-    const uint64_t pol = ptx::l2_policy_evict_first();
-#pragma unroll
-    for (int i = 0; i < 8; ++i) ptx::st_global_v8_hint(out + 32 * i, pk + 8 * i, pol);
-  } else if (kMode != kModeGeneral || __builtin_expect(p.o_align32, 1)) {   // 32-byte stores where allowed
+  if (__builtin_expect(p.o_align32, 1)) {   // 32-byte stores where allowed
 #pragma unroll
     for (int i = 0; i < 8; ++i) ptx::st_global_v8(out + 32 * i, pk + 8 * i);
   } else {
@@ -1040,10 +1036,10 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
     if (have_prev) {
       if (kSplit && sp.slot >= 0) {
         if (!epilogue_split(c, split_out(p), q, sp, row, m_prev, l_prev, lr_prev, o_parity)) return;
-      } else if (kMode == kModeGeneral) {
+      } else if constexpr (kMode == kModeGeneral) {
         uint32_t pk[64];
         if (!epilogue_read(c, q, o_parity, 1.0f / lr_prev, pk)) return;
-        epilogue_store<kMode>(p, q, sp.w, row, m_prev, l_prev, pk);
+        epilogue_store(p, q, sp.w, row, m_prev, l_prev, pk);
       }
       o_parity ^= 1u;
     }
@@ -1113,13 +1109,13 @@ __device__ __forceinline__ void softmax_role(const Ctx& c, const Params& p, int 
     l_prev = l;
     lr_prev = l + dl;
   }
-  if (have_prev && ((kSplit && sp.slot >= 0) || kMode == kModeGeneral)) {
+  if (have_prev) {
     if (kSplit && sp.slot >= 0) {
       epilogue_split(c, split_out(p), q, sp, row, m_prev, l_prev, lr_prev, o_parity);
-    } else {
+    } else if constexpr (kMode == kModeGeneral) {
       uint32_t pk[64];
       if (!epilogue_read(c, q, o_parity, 1.0f / lr_prev, pk)) return;
-      epilogue_store<kMode>(p, q, sp.w, row, m_prev, l_prev, pk);
+      epilogue_store(p, q, sp.w, row, m_prev, l_prev, pk);
     }
   }
 }
