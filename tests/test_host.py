@@ -387,3 +387,16 @@ def test_workspace_query_needs_no_launch(lib):
     assert attn.workspace_bytes(0, 16, 4096, 4096) == 0
     with pytest.raises(attn.AttnError):
         attn.workspace_bytes(1, 1, 128, 128, D=64)
+
+
+def test_bench_config_names_each_rows_mask_and_layout():
+    # the JSON line's per-shape config states the row's causal flag and tensor layout
+    import bench
+    from dense_attention_forward_attn_gb300 import workloads as wl
+    dense = bench.bench_config("w", wl.HEADLINE, 24, 1)
+    assert [d["causal"] for d in dense["shapes"]] == [False] * len(wl.HEADLINE)
+    assert {d["layout"] for d in dense["shapes"]} == {"BHSD contiguous"}
+    causal = bench.bench_config("w", wl.HEADLINE, 24, 1, causal=True, layout="bshd")
+    assert all(d["causal"] for d in causal["shapes"])
+    assert {d["layout"] for d in causal["shapes"]} == {"BSHD contiguous"}
+    assert causal["parallelism"] == "single GPU" and dense["problems_per_shape_per_step"] == 24
