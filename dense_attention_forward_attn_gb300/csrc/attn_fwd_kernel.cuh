@@ -415,11 +415,13 @@ __device__ __forceinline__ void load_role(const Ctx& c, const Params& p, const C
       ptx::tma_load_3d(dst, tm, fb, col, row, bh);
     }
   };
-  // Causal mode: the heaviest-first order keeps every head's K/V in use for the whole launch,
-  // more than L2 holds at S=4K (B=4, H=16: 128 MiB); Q tiles, read once, are marked first to
-  // evict so they do not push K/V lines out (+1.0% at causal S=4K, +0.6% at S=16K).
+  // Q tiles, read once, are marked first to evict from L2 so they do not push K/V lines out
+  // (re-read by every item of a head).  Causal mode, where the heaviest-first order keeps every
+  // head's K/V in use for the whole launch (128 MiB at S=4K, B=4, H=16): +1.0% at causal S=4K,
+  // +0.6% at S=16K; full-tile mode, with O stored the same way: +0.0 / +0.6 / +0.6% at
+  // S=4K/8K/16K.
   auto load_q_box = [&](uint32_t dst, uint32_t fb, int col, int row, int bh) {
-    if (kMode != kModeCausal) {
+    if (kMode == kModeGeneral) {
       load_box(dst, tm_q, fb, col, row, bh);
     } else if (kBshd) {
       const int b = bh / p.heads, h = bh - b * p.heads;
@@ -1165,8 +1167,7 @@ __device__ __forceinline__ void correction_role(const Ctx& c, const Params& p) {
 #pragma unroll
       for (int i = 0; i < 8; ++i)
         pk[i] = ptx::pack_bf16x2(__uint_as_float(v[2 * i]) * f.x, __uint_as_float(v[2 * i + 1]) * f.x);
-      if (kMode == kModeCausal) ptx::st_global_v8_hint(out + 32 * cc, pk, pol);
-      else ptx::st_global_v8(out + 32 * cc, pk);
+      ptx::st_global_v8_hint(out + 32 * cc, pk, pol);   // written once: first to evict from L2
     }
     if (p.lse != nullptr) p.lse[static_cast<size_t>(w.bh) * p.sq + grow] = f.y;
     ptx::tc_fence_before();
